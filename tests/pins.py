@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` function takes the oracle module and raises AssertionError when
+the oracle disagrees with
+  * brute-force pure-Python loops on tiny inputs,
+  * library routines in float64 (torch's scaled_dot_product_attention,
+    F.linear, F.gelu, F.silu, the bf16 cast),
+  * closed forms (causal first row, equal keys, zero weights, Phi(1), ...),
+  * identities the pages fix (column-parallel concat, row-parallel partial
+    sums, per-head concat, degree invariance of the whole block),
+  * the degree-rule table in ``golden/plan_rules.json``.
+``test_oracle_mutations.py`` plants plausible mistakes in the oracle and
+checks that at least one pin catches each.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _weights(rng, d, f, act, std=0.3):
+    w = {n: rng.standard_normal((d, d)) * std for n in ("Wq", "Wk", "Wv", "Wo")}
+    if act == "swiglu":
+        w["Wg"] = rng.standard_normal((f, d)) * std
+        w["Wu"] = rng.standard_normal((f, d)) * std
+    else:
+        w["W1"] = rng.standard_normal((f, d)) * std
+    w["Wd"] = rng.standard_normal((d, f)) * std
+    return w
+
+
+# ----------------------------------------------------------------------------
+# brute force (pure Python loops, nothing shared with the oracle)
+# ----------------------------------------------------------------------------
+
+def bf_matvec_rows(x, W):
+    T, K = len(x), len(x[0])
+    return [[sum(x[t][k] * W[o][k] for k in range(K)) for o in range(len(W))] for t in range(T)]
+
+
+def bf_gelu(v):
+    return 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
+
+
+def bf_silu(v):
+    return v / (1.0 + math.exp(-v))
+
+
+def bf_block_seq(x, w, H, act, causal, kc=None, vc=None, P=0, rnd=None):
+    """One sequence.  x: list of T rows of d floats.  kc/vc: [H][P][dh] lists.
+    ``rnd`` (optional) rounds a scalar at the bf16 storage points."""
+    r = rnd or (lambda v: v)
+    T, d = len(x), len(x[0])
+    dh = d // H
+    q = [[r(v) for v in row] for row in bf_matvec_rows(x, w["Wq"])]
+    k = [[r(v) for v in row] for row in bf_matvec_rows(x, w["Wk"])]
+    v_ = [[r(v) for v in row] for row in bf_matvec_rows(x, w["Wv"])]
+    # full key/value rows: cache rows first (positions 0..P-1), then new tokens
+    keys, vals = [], []
+    for p in range(P):
+        keys.append([kc[h][p][c] for h in range(H) for c in range(dh)])
+        vals.append([vc[h][p][c] for h in range(H) for c in range(dh)])
+    keys += k
+    vals += v_
+    a = [[0.0] * d for _ in range(T)]
+    for h in range(H):
+        for i in range(T):
+            qpos = P + i
+            js = [j for j in range(len(keys)) if (not causal or j <= qpos)]
+            s = [sum(q[i][h * dh + c] * keys[j][h * dh + c] for c in range(dh)) / math.sqrt(dh) for j in js]
+            m = max(s)
+            e = [math.exp(t - m) for t in s]
+            z = sum(e)
+            for c in range(dh):
+                a[i][h * dh + c] = sum(e[n] * vals[js[n]][h * dh + c] for n in range(len(js))) / z
+    a = [[r(v) for v in row] for row in a]
+    o = bf_matvec_rows(a, w["Wo"])
+    hres = [[x[t][c] + o[t][c] for c in range(d)] for t in range(T)]
+    hop = [[r(v) for v in row] for row in hres]
+    if act == "swiglu":
+        g = bf_matvec_rows(hop, w["Wg"])
+        u_ = bf_matvec_rows(hop, w["Wu"])
+        u = [[bf_silu(g[t][n]) * u_[t][n] for n in range(len(g[0]))] for t in range(T)]
+    else:
+        g = bf_matvec_rows(hop, w["W1"])
+        u = [[bf_gelu(g[t][n]) for n in range(len(g[0]))] for t in range(T)]
+    u = [[r(v) for v in row] for row in u]
+    dn = bf_matvec_rows(u, w["Wd"])
+    return [[hres[t][c] + dn[t][c] for c in range(d)] for t in range(T)]
+
+
+def _tolist(w):
+    return {n: a.tolist() for n, a in w.items()}
+
+
+# ----------------------------------------------------------------------------
+# pins
+# ----------------------------------------------------------------------------
+
+def pin_brute_force_block(o):
+    for act in ("gelu", "swiglu"):
+        for causal in (False, True):
+            rng = _rng(1 + causal + 2 * (act == "gelu"))
+            B, T, d, H, f = 2, 5, 8, 2, 12
+            w = _weights(rng, d, f, act)
+            x = rng.standard_normal((B, T, d))
+            Y, _, _ = o.block_forward(x, w, H, act, causal)
+            wl = _tolist(w)
+            for b in range(B):
+                ref = np.array(bf_block_seq(x[b].tolist(), wl, H, act, causal))
+                assert np.max(np.abs(Y[b] - ref)) < 1e-12, (act, causal)
+
+
+def pin_brute_force_cached(o):
+    """Tokens at positions P.. over a filled cache (decode and chunked prefill)."""
+    for T, causal in ((1, True), (3, True), (2, False)):
+        rng = _rng(7 + T)
+        B, d, H, f, P, cap = 2, 8, 2, 6, 4, 9
+        dh = d // H
+        w = _weights(rng, d, f, "swiglu")
+        x = rng.standard_normal((B, T, d))
+        kc = rng.standard_normal((B, H, cap, dh))
+        vc = rng.standard_normal((B, H, cap, dh))
+        Y, Kn, Vn = o.block_forward(x, w, H, "swiglu", causal, kc, vc, P)
+        wl = _tolist(w)
+        for b in range(B):
+            ref = np.array(bf_block_seq(x[b].tolist(), wl, H, "swiglu", causal,
+                                        kc[b].tolist(), vc[b].tolist(), P))
+            assert np.max(np.abs(Y[b] - ref)) < 1e-12, (T, causal)
+            kref = x[b] @ w["Wk"].T
+            assert np.max(np.abs(Kn[b].transpose(1, 0, 2).reshape(T, d) - kref)) < 1e-12
+
+
+def pin_brute_force_bf16_storage(o):
+    """The bf16 storage mode equals brute force with torch's bf16 cast at the
+    same points (Q/K/V, attention output, H operand, U)."""
+    def rnd(v):
+        return float(torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).double())
+    for act in ("gelu", "swiglu"):
+        rng = _rng(31 + (act == "gelu"))
+        B, T, d, H, f = 1, 4, 8, 2, 8
+        w = _weights(rng, d, f, act)
+        x = rng.standard_normal((B, T, d))
+        Y, _, _ = o.block_forward(x, w, H, act, True, storage="bf16")
+        ref = np.array(bf_block_seq(x[0].tolist(), _tolist(w), H, act, True, rnd=rnd))
+        # H keeps an fp32 copy for the residual: compare at fp32 resolution
+        assert np.max(np.abs(Y[0] - ref)) < 1e-5 * max(1.0, np.max(np.abs(ref)))
+        Y0, _, _ = o.block_forward(x, w, H, act, True)
+        assert np.max(np.abs(Y - Y0)) > 1e-6  # the mode really rounds
+
+
+def pin_torch_attention(o):
+    """Per-head attention equals torch's scaled_dot_product_attention (fp64)."""
+    rng = _rng(3)
+    for causal in (False, True):
+        for T, H, dh in ((33, 4, 16), (70, 2, 64), (1, 3, 8)):
+            q, k, v = (rng.standard_normal((T, H * dh)) for _ in range(3))
+            out = o.multi_head_attention(q, k, v, H, causal)
+            tq, tk, tv = (torch.from_numpy(a.reshape(T, H, dh).transpose(1, 0, 2).copy()) for a in (q, k, v))
+            ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal)
+            ref = ref.numpy().transpose(1, 0, 2).reshape(T, H * dh)
+            assert np.max(np.abs(out - ref)) < 1e-12, (causal, T, H, dh)
+
+
+def pin_torch_activations(o):
+    x = np.concatenate([np.linspace(-40, 40, 4001), _rng(5).standard_normal(1000) * 3])
+    tx = torch.from_numpy(x)
+    assert np.max(np.abs(o.gelu_erf(x) - F.gelu(tx, approximate="none").numpy())) < 1e-12
+    assert np.max(np.abs(o.silu(x) - F.silu(tx).numpy())) < 1e-12
+
+
+def pin_torch_linear(o):
+    rng = _rng(6)
+    x, W = rng.standard_normal((7, 13)), rng.standard_normal((5, 13))
+    ref = F.linear(torch.from_numpy(x), torch.from_numpy(W)).numpy()
+    assert np.max(np.abs(o.linear(x, W) - ref)) < 1e-12
+
+
+def pin_column_parallel(o):
+    """Concatenating the column-parallel shards gives the full product."""
+    rng = _rng(8)
+    x, W = rng.standard_normal((9, 24)), rng.standard_normal((40, 24))
+    full = x @ W.T
+    for tp in (1, 2, 4, 8):
+        shards = o.column_parallel_linear(x, W, tp)
+        assert len(shards) == tp and shards[0].shape == (9, 40 // tp)
+        assert np.max(np.abs(np.concatenate(shards, axis=1) - full)) < 1e-12
+
+
+def pin_row_parallel(o):
+    """Summing the row-parallel partials gives the full product."""
+    rng = _rng(9)
+    x, W = rng.standard_normal((9, 32)), rng.standard_normal((12, 32))
+    full = x @ W.T
+    for tp in (1, 2, 4, 8):
+        parts = o.row_parallel_partials(x, W, tp)
+        assert len(parts) == tp and parts[0].shape == full.shape
+        if tp > 1:
+            assert np.max(np.abs(parts[0] - full)) > 1e-3  # a partial is not the whole
+        assert np.max(np.abs(o.all_reduce_sum(parts) - full)) < 1e-12
+
+
+def pin_head_concat(o):
+    """Attention over shard-owned head groups, concatenated, is the unsharded MHA."""
+    rng = _rng(10)
+    T, H, dh = 11, 8, 4
+    q, k, v = (rng.standard_normal((T, H * dh)) for _ in range(3))
+    full = o.multi_head_attention(q, k, v, H, True)
+    for tp in (1, 2, 4, 8):
+        h_l = H // tp
+        parts = []
+        for s in range(tp):
+            c = slice(s * h_l * dh, (s + 1) * h_l * dh)
+            parts.append(o.multi_head_attention(q[:, c], k[:, c], v[:, c], h_l, True))
+        assert np.max(np.abs(np.concatenate(parts, axis=1) - full)) < 1e-12
+
+
+def pin_degree_invariance(o):
+    """The block computed shard by shard equals the unsharded block for every
+    degree 1, 2, 4, 8."""
+    for act in ("swiglu", "gelu"):
+        rng = _rng(11 + (act == "gelu"))
+        B, T, d, H, f = 2, 6, 32, 8, 24
+        w = _weights(rng, d, f, act)
+        x = rng.standard_normal((B, T, d))
+        Y, _, _ = o.block_forward(x, w, H, act, True)
+        for tp in (1, 2, 4, 8):
+            Ys, A, U = o.sharded_block_forward(x, w, H, act, True, tp)
+            assert len(A[0]) == tp and A[0][0].shape == (T, d // tp)
+            assert len(U[0]) == tp and U[0][0].shape == (T, f // tp)
+            assert np.max(np.abs(Ys - Y)) < 1e-11, (act, tp)
+
+
+def pin_closed_forms_attention(o):
+    rng = _rng(12)
+    T, dh = 6, 4
+    q, k, v = (rng.standard_normal((T, dh)) for _ in range(3))
+    # the first query under a causal mask sees only key 0
+    assert np.max(np.abs(o.attention_head(q, k, v, True)[0] - v[0])) < 1e-15
+    # equal keys: uniform weights, the output is the mean of the visible values
+    kk = np.tile(k[:1], (T, 1))
+    out = o.attention_head(q, kk, v, False)
+    assert np.max(np.abs(out - v.mean(axis=0))) < 1e-12
+    outc = o.attention_head(q, kk, v, True)
+    run = np.cumsum(v, axis=0) / np.arange(1, T + 1)[:, None]
+    assert np.max(np.abs(outc - run)) < 1e-12
+    # two keys whose scaled scores differ by ln 3: weights 1/4 and 3/4
+    q1 = np.array([[2.0 * math.log(3.0), 0.0, 0.0, 0.0]])
+    k2 = np.array([[0.0, 0, 0, 0], [1.0, 0, 0, 0]])
+    v2 = np.array([[4.0, 0, 0, 0], [0.0, 8.0, 0, 0]])
+    assert np.max(np.abs(o.attention_head(q1, k2, v2, False)[0] - np.array([1.0, 6.0, 0, 0]))) < 1e-12
+    # a large score difference picks the value of that key
+    q3 = np.array([[200.0, 0, 0, 0]])
+    assert np.max(np.abs(o.attention_head(q3, k2, v2, False)[0] - v2[1])) < 1e-12
+    # softmax: rows sum to one; logs of 1,2,3 give 1/6, 2/6, 3/6
+    p = o.softmax_rows(np.log(np.array([[1.0, 2.0, 3.0], [5.0, 5.0, 5.0]])))
+    assert np.max(np.abs(p - np.array([[1 / 6, 2 / 6, 3 / 6], [1 / 3] * 3]))) < 1e-15
+    p = o.softmax_rows(rng.standard_normal((5, 9)) * 30)
+    assert np.max(np.abs(p.sum(axis=1) - 1)) < 1e-14
+
+
+def pin_closed_forms_activations(o):
+    # Phi(1) = 0.841344746068542948... (standard normal CDF), so gelu(1) = Phi(1)
+    assert abs(o.gelu_erf(np.array([1.0]))[0] - 0.8413447460685429) < 1e-15
+    assert abs(o.gelu_erf(np.array([-1.0]))[0] + (1 - 0.8413447460685429)) < 1e-15
+    # sigmoid(ln 3) = 3/4
+    assert abs(o.silu(np.array([math.log(3.0)]))[0] - 0.75 * math.log(3.0)) < 1e-15
+    assert o.gelu_erf(np.array([0.0]))[0] == 0.0 and o.silu(np.array([0.0]))[0] == 0.0
+    assert abs(o.gelu_erf(np.array([30.0]))[0] - 30.0) < 1e-12
+    assert abs(o.silu(np.array([-60.0]))[0]) < 1e-20
+
+
+def pin_closed_forms_block(o):
+    """Zero output projections leave Y = X; zero attention weights give the
+    running mean of V under a causal mask."""
+    rng = _rng(13)
+    B, T, d, H, f = 1, 5, 8, 2, 4
+    w = _weights(rng, d, f, "swiglu")
+    x = rng.standard_normal((B, T, d))
+    w0 = dict(w, Wo=np.zeros((d, d)), Wd=np.zeros((d, f)))
+    Y, _, _ = o.block_forward(x, w0, H, "swiglu", True)
+    assert np.max(np.abs(Y - x)) == 0.0
+    # Wq = 0 -> every visible key scores 0 -> attention = running mean of V
+    wq0 = dict(w, Wq=np.zeros((d, d)), Wd=np.zeros((d, f)))
+    Y, _, _ = o.block_forward(x, wq0, H, "swiglu", True)
+    vv = x[0] @ w["Wv"].T
+    run = np.cumsum(vv, axis=0) / np.arange(1, T + 1)[:, None]
+    assert np.max(np.abs(Y[0] - (x[0] + run @ w["Wo"].T))) < 1e-12
+
+
+def pin_decode_equals_prefill(o):
+    """Running the last token over a cache of the earlier tokens' K/V gives the
+    prefill's last row, and the appended K/V."""
+    rng = _rng(14)
+    B, T, d, H, f = 2, 7, 16, 4, 8
+    w = _weights(rng, d, f, "swiglu")
+    x = rng.standard_normal((B, T, d))
+    Y, K, V = o.block_forward(x, w, H, "swiglu", True)
+    cap = 10
+    kc = np.zeros((B, H, cap, d // H))
+    vc = np.zeros((B, H, cap, d // H))
+    kc[:, :, :T - 1] = K[:, :, :T - 1]
+    vc[:, :, :T - 1] = V[:, :, :T - 1]
+    Yd, Kd, Vd = o.block_forward(x[:, T - 1:], w, H, "swiglu", True, kc, vc, T - 1)
+    assert np.max(np.abs(Yd[:, 0] - Y[:, T - 1])) < 1e-12
+    assert np.max(np.abs(Kd[:, :, 0] - K[:, :, T - 1])) < 1e-12
+    assert np.max(np.abs(Vd[:, :, 0] - V[:, :, T - 1])) < 1e-12
+
+
+def pin_round_bf16(o):
+    # ties to even at 1: 1 + 2^-8 -> 1, 1 + 3*2^-8 -> 1 + 2^-6
+    vals = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3.0, 0.0, 1e-30])
+    exp = np.array([1.0, 1 + 2.0 ** -6, -1.0, 3.0, 0.0, None], dtype=object)
+    got = o.round_bf16(vals)
+    for g, e in zip(got[:5], exp[:5]):
+        assert g == e
+    # against torch's fp32 -> bf16 cast (round to nearest even)
+    x = (_rng(15).standard_normal(200000) * np.exp(_rng(16).uniform(-20, 20, 200000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.round_bf16(x.astype(np.float64)), ref)
+
+
+def pin_plan_rules(o):
+    with open(os.path.join(GOLDEN, "plan_rules.json")) as fh:
+        table = json.load(fh)
+    for c in table["cases"]:
+        got = o.check_plan(c["d_model"], c["n_heads"], c["d_ffn"], c["tp"])
+        assert got == c["expect"], (c, got)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,131 @@
+"""Plants plausible mistakes in the CPU oracle (on the CPU, through
+monkeypatch) and checks that the pins catch every one of them."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.tp_oracle as o
+from pins import ALL_PINS
+
+real = {n: getattr(o, n) for n in ("attention_head", "linear", "silu", "gelu_erf", "all_reduce_sum",
+                                   "block_forward", "round_bf16", "check_plan", "multi_head_attention",
+                                   "softmax_rows", "row_parallel_partials", "column_parallel_linear",
+                                   "sharded_block_forward")}
+
+
+def _att_scale_dh(q, k, v, causal, q_pos0=0):
+    q, k, v = o.to64(q), o.to64(k), o.to64(v)
+    return real["attention_head"](q / math.sqrt(q.shape[-1]), k, v, causal, q_pos0)  # 1/d instead of 1/sqrt(d)
+
+
+def _att_mask_shift(q, k, v, causal, q_pos0=0):
+    return real["attention_head"](q, k, v, causal, q_pos0 - 1 if causal else q_pos0)
+
+
+def _att_no_mask(q, k, v, causal, q_pos0=0):
+    return real["attention_head"](q, k, v, False, q_pos0)
+
+
+def _lt(x, W):
+    W = o.to64(W)
+    x = o.to64(x)
+    if W.shape[0] == W.shape[1]:
+        return x @ W  # a square weight used untransposed
+    return x @ W.T
+
+
+def _silu_sign(x):
+    x = o.to64(x)
+    return x / (1.0 + np.exp(x))
+
+
+def _gelu_tanh(x):
+    x = o.to64(x)
+    return 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))
+
+
+def _reduce_drop_last(parts):
+    return real["all_reduce_sum"](parts[:-1]) if len(parts) > 1 else parts[0]
+
+
+def _block_no_residual(x, w, H, act, causal, *a, **kw):
+    Y, K, V = real["block_forward"](x, w, H, act, causal, *a, **kw)
+    return Y - o.to64(x), K, V
+
+
+def _round_truncate(a):
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32) & np.uint32(0xFFFF0000)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _plan_no_ffn(d, H, f, tp):
+    r = real["check_plan"](d, H, f, tp)
+    return "OK" if r == "FFN_NOT_DIVISIBLE" else r
+
+
+def _plan_le(d, H, f, tp):
+    r = real["check_plan"](d, H, f, tp)
+    return "OK" if (r == "DEGREE_RANGE" and tp >= 1) else r
+
+
+def _mha_wrong_head_cols(q, k, v, n_heads, causal, q_pos0=0):
+    # heads taken as interleaved columns instead of contiguous blocks
+    q, k, v = o.to64(q), o.to64(k), o.to64(v)
+    outs = []
+    for j in range(n_heads):
+        c = slice(j, None, n_heads)
+        outs.append(real["attention_head"](q[:, c], k[:, c], v[:, c], causal, q_pos0))
+    return np.concatenate(outs, axis=-1)
+
+
+def _softmax_no_max(s):
+    s = o.to64(s)
+    e = np.exp(np.where(np.isinf(s), -np.inf, s))
+    return e / np.sum(e, axis=-1, keepdims=True) * (1 + 1e-9)
+
+
+def _row_wrong_block(x, W, tp):
+    x, W = o.to64(x), o.to64(W)
+    k = W.shape[1] // tp
+    return [x[..., s * k:(s + 1) * k] @ W[:, ((s + 1) % tp) * k:((s + 1) % tp + 1) * k].T for s in range(tp)]
+
+
+def _col_wrong(x, W, tp):
+    W = o.to64(W)
+    n = W.shape[0] // tp
+    return [o.linear(x, W[s::tp][:n]) for s in range(tp)]
+
+
+MUTATIONS = {
+    "attention scale 1/d": ("attention_head", _att_scale_dh),
+    "causal mask off by one": ("attention_head", _att_mask_shift),
+    "causal mask dropped": ("attention_head", _att_no_mask),
+    "square weight not transposed": ("linear", _lt),
+    "silu sign": ("silu", _silu_sign),
+    "gelu tanh form": ("gelu_erf", _gelu_tanh),
+    "all-reduce drops a partial": ("all_reduce_sum", _reduce_drop_last),
+    "residual dropped": ("block_forward", _block_no_residual),
+    "bf16 truncation": ("round_bf16", _round_truncate),
+    "FFN divisibility unchecked": ("check_plan", _plan_no_ffn),
+    "degree range unchecked": ("check_plan", _plan_le),
+    "heads as interleaved columns": ("multi_head_attention", _mha_wrong_head_cols),
+    "softmax slightly off": ("softmax_rows", _softmax_no_max),
+    "row-parallel mismatched blocks": ("row_parallel_partials", _row_wrong_block),
+    "column-parallel strided slices": ("column_parallel_linear", _col_wrong),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    attr, bad = MUTATIONS[name]
+    monkeypatch.setattr(o, attr, bad)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(o)
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake: {name}"
