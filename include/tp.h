@@ -1,0 +1,217 @@
+/*
+ * tp.h -- C ABI of the tensor-parallel transformer block on one GPU.
+ *
+ * The block is the Megatron-style decomposition described on
+ * undercodenews.com/?p=110319, section "the Original": Q/K/V and the first
+ * FFN linear are column-parallel (every shard multiplies the full input by
+ * its slice of the output features, so shard s owns heads
+ * [s*H/tp, (s+1)*H/tp)), attention runs per shard over its own heads, and
+ * the output projection and the second FFN linear are row-parallel, their
+ * per-shard partial products being summed by an all-reduce.  Here all tp
+ * shards are logical partitions of one GPU's memory and the all-reduce is a
+ * sum of the partials inside the row-parallel GEMM's accumulator.
+ *
+ * Block computed by tp_block_forward (residuals, activation, mask and scale
+ * are readings where the pages are silent; the design notes list them):
+ *     Q, K, V = X Wq^T, X Wk^T, X Wv^T                 (column-parallel, by head)
+ *     A       = concat_j softmax(Q_j K_j^T / sqrt(d_head) + mask) V_j
+ *     H       = X + sum_s A_s Wo_s^T                    (row-parallel + reduce)
+ *     U       = silu(H Wg^T) * (H Wu^T)   or  gelu(H W1^T)   (column-parallel)
+ *     Y       = H + sum_s U_s Wd_s^T                    (row-parallel + reduce)
+ *
+ * Conventions shared by every call:
+ *  - Pointers named "device" point to device memory owned by the caller; the
+ *    library never allocates device memory and never frees caller memory.
+ *    A plan owns only host metadata (and cached TMA descriptors).
+ *  - Matrices are row-major.  Weights use the [out_features, in_features]
+ *    layout.  M = batch * seq tokens; token t of sequence b is row b*seq + t.
+ *  - "act" tensors have the plan's storage dtype (bf16 or fp32); fp32 tensors
+ *    are always fp32.  bf16 is IEEE bfloat16 (round to nearest even).
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Every call only enqueues work and returns; results are ready
+ *    when the stream reaches them.
+ *  - Arguments are validated on the host before anything is enqueued; a call
+ *    that returns an error has enqueued nothing.  Device pointers must be
+ *    16-byte aligned (TP_ERR_ALIGNMENT otherwise).  Launch failures return
+ *    TP_ERR_CUDA.  Device-side bounded waits that give up record a code that
+ *    tp_sync_status() reports as TP_ERR_DEVICE_TIMEOUT.
+ *  - A plan is immutable after creation and may be used from several host
+ *    threads and streams at once, provided calls in flight at the same time
+ *    do not share output or workspace buffers.
+ */
+#ifndef TP_H_
+#define TP_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tp_plan_s* tp_plan_t;
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_NULL_ARG = 1,              /* a required pointer is NULL            */
+    TP_ERR_INVALID_DIM = 2,           /* a dimension or size is <= 0 / out of range */
+    TP_ERR_DEGREE_RANGE = 3,          /* tp_degree < 1 or tp_degree > n_heads  */
+    TP_ERR_HEADS_NOT_DIVISIBLE = 4,   /* n_heads % tp_degree != 0              */
+    TP_ERR_FFN_NOT_DIVISIBLE = 5,     /* d_ffn % tp_degree != 0                */
+    TP_ERR_DMODEL_NOT_DIVISIBLE = 6,  /* d_model % n_heads != 0                */
+    TP_ERR_ALIGNMENT = 7,             /* pointer not 16-byte aligned, or a width
+                                         not a multiple of 8 elements          */
+    TP_ERR_WORKSPACE_TOO_SMALL = 8,
+    TP_ERR_UNSUPPORTED = 9,           /* valid plan, shape this build has no kernel for */
+    TP_ERR_CUDA = 10,                 /* a CUDA runtime/launch error           */
+    TP_ERR_DEVICE_TIMEOUT = 11        /* a device-side bounded wait gave up    */
+} tp_status;
+
+typedef enum { TP_ACT_GELU = 0, TP_ACT_SWIGLU = 1 } tp_act;
+typedef enum { TP_BF16 = 0, TP_FP32 = 1 } tp_dtype;
+typedef enum { TP_QKV = 0, TP_FFN_UP = 1 } tp_column_which;
+typedef enum { TP_ATTN_OUT = 0, TP_FFN_DOWN = 1 } tp_row_which;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tp_status_string(tp_status s);
+
+/* Text of the last CUDA error that made a call on this host thread return
+ * TP_ERR_CUDA ("" if none).  Thread-local storage owned by the library. */
+const char* tp_last_cuda_error(void);
+
+/*
+ * Create a plan.  Degree rule from undercodenews.com/?p=110319, "the
+ * Original" (degree <= head count, head count and FFN width divisible by
+ * the degree) and "What Is Tensor Parallelism?" (netray.co), "Tensor
+ * Parallelism Explained".  Checks, first failure returned:
+ *   d_model, n_heads, d_ffn > 0            else TP_ERR_INVALID_DIM
+ *   tp_degree >= 1                         else TP_ERR_DEGREE_RANGE
+ *   d_model % n_heads == 0                 else TP_ERR_DMODEL_NOT_DIVISIBLE
+ *   tp_degree <= n_heads                   else TP_ERR_DEGREE_RANGE
+ *   n_heads % tp_degree == 0               else TP_ERR_HEADS_NOT_DIVISIBLE
+ *   d_ffn % tp_degree == 0                 else TP_ERR_FFN_NOT_DIVISIBLE
+ * then the storage constraint of this build: d_model, d_head and d_ffn/tp
+ * multiples of 8 (TP_ERR_ALIGNMENT), so that every row starts 16-byte
+ * aligned.  An unknown act/dtype gives TP_ERR_UNSUPPORTED.
+ * tp_plan_create uses SwiGLU and bf16.  On error *out is set to NULL.
+ * Host only: touches no GPU.
+ */
+tp_status tp_plan_create(int d_model, int n_heads, int d_ffn, int tp_degree, tp_plan_t* out);
+tp_status tp_plan_create_ex(int d_model, int n_heads, int d_ffn, int tp_degree,
+                            tp_act act, tp_dtype dtype, tp_plan_t* out);
+void tp_plan_destroy(tp_plan_t plan);
+
+/*
+ * Bytes the caller must provide: the packed shard-major weights (written by
+ * tp_shard_weights) and the workspace tp_block_forward needs for `batch`
+ * sequences of `seq` new tokens.  Either output pointer may be NULL.
+ */
+tp_status tp_plan_sizes(tp_plan_t plan, int batch, int seq,
+                        size_t* packed_weight_bytes, size_t* workspace_bytes);
+
+/* Bytes of scratch tp_attention_heads needs for this call shape (0 for
+ * prefill-shaped calls; split-KV partials for single-token decode). */
+tp_status tp_attention_scratch_bytes(tp_plan_t plan, int batch, int seq_q, int cache_cap,
+                                     size_t* bytes);
+
+/*
+ * Pack full weights (device, plan dtype, [out, in] row-major) into the
+ * shard-major layout the kernels read (device, `packed`, at least
+ * packed_weight_bytes).  Shard s receives: the Q, K and V rows of its heads
+ * (column-parallel by head); the columns of Wo that meet its heads
+ * (row-parallel); its d_ffn/tp rows of Wg and Wu interleaved in blocks of g
+ * rows (g gate rows, the g matching up rows, ...; g = 32 when d_ffn/tp is a
+ * multiple of 32, else 16, else 8) or its rows of W1; its d_ffn/tp columns
+ * of Wd.  Wup must be NULL for GELU plans and non-NULL for SwiGLU plans.
+ */
+tp_status tp_shard_weights(tp_plan_t plan, const void* Wq, const void* Wk, const void* Wv,
+                           const void* Wo, const void* W1_or_Wgate, const void* Wup,
+                           const void* Wdown, void* packed, void* stream);
+
+/*
+ * Column-parallel linear over all shards in one launch
+ * (undercodenews.com/?p=110319, "the Original": each shard multiplies the
+ * full input by its slice of the output features).
+ *   x          device act [M, d_model]
+ *   out_shards device act [tp][M][n_s], where
+ *      TP_QKV:    n_s = 3*h_l*d_head, row = [Q of its h_l heads | K | V],
+ *                 each head's d_head columns contiguous, heads in order;
+ *      TP_FFN_UP: n_s = d_ffn/tp, the activated U_s = silu(x Wg_s^T) *
+ *                 (x Wu_s^T) (SwiGLU) or gelu(x W1_s^T) (GELU, erf form).
+ * M >= 1.
+ */
+tp_status tp_column_linear(tp_plan_t plan, int which, const void* x, int M,
+                           const void* packed, void* out_shards, void* stream);
+
+/*
+ * Row-parallel linear with the all-reduce fused in (same page and section:
+ * the input's column blocks meet the weight's matching row blocks and the
+ * partials are summed).  Computes
+ *   out_f32[M, d] = residual + sum_{s=0}^{tp-1} in_shards[s] W_s^T
+ * with the shard partials accumulated in fp32, in shard order, in the
+ * GEMM's accumulator -- no partial ever goes to memory.
+ *   in_shards  device act [tp][M][k_s]; k_s = h_l*d_head (TP_ATTN_OUT) or
+ *              d_ffn/tp (TP_FFN_DOWN)
+ *   residual   device, nullable, [M, d]: plan dtype for TP_ATTN_OUT (the
+ *              block input), fp32 for TP_FFN_DOWN (H)
+ *   out_f32    device fp32 [M, d]
+ *   out_act    device act [M, d], nullable: a copy of out_f32 in the plan
+ *              dtype (the operand of the next column-parallel linear)
+ */
+tp_status tp_row_linear_reduce(tp_plan_t plan, int which, const void* in_shards, int M,
+                               const void* packed, const void* residual, void* out_f32,
+                               void* out_act, void* stream);
+
+/*
+ * Per-shard multi-head attention over each shard's own heads
+ * (undercodenews.com/?p=110319, "the Original": every head attends
+ * independently, no communication).  For each sequence b, shard s and local
+ * head j (global head h = s*h_l + j):
+ *   O = softmax(Q K^T / sqrt(d_head) + mask) V
+ * The seq_q query tokens sit at positions cache_pos .. cache_pos+seq_q-1.
+ * With causal != 0 a query at position p sees keys at positions <= p.
+ *   qkv_shards  device act [tp][batch*seq_q][3*h_l*d_head] (tp_column_linear
+ *               TP_QKV layout)
+ *   k_cache, v_cache  device act [batch][n_heads][cache_cap][d_head], or both
+ *               NULL.  When given, the new tokens' K and V are written at
+ *               positions cache_pos.. and attention runs over positions
+ *               0 .. cache_pos+seq_q-1 of the cache ("Tensor Parallelism:
+ *               Splitting One Layer Across GPUs" (byteledger), "Interaction
+ *               with the rest of serving": the KV cache is split with the
+ *               heads -- head h's cache rows belong to its shard).  When
+ *               NULL, cache_pos must be 0 and the seq_q tokens attend among
+ *               themselves.
+ *   out_shards  device act [tp][batch*seq_q][h_l*d_head]
+ *   scratch     device, scratch_bytes >= tp_attention_scratch_bytes(); may be
+ *               NULL when that is 0.  Contents on entry are ignored.
+ */
+tp_status tp_attention_heads(tp_plan_t plan, const void* qkv_shards, int batch, int seq_q,
+                             int causal, void* k_cache, void* v_cache, int cache_cap,
+                             int cache_pos, void* out_shards, void* scratch,
+                             size_t scratch_bytes, void* stream);
+
+/*
+ * The whole block: column QKV, attention, row O + reduce (+x), column
+ * FFN-up + activation, row FFN-down + reduce (+H).
+ *   x         device act [batch*seq][d_model]
+ *   k_cache/v_cache/cache_cap/cache_pos   as in tp_attention_heads
+ *   packed    device, from tp_shard_weights
+ *   workspace device, ws_bytes >= tp_plan_sizes(batch, seq) workspace bytes
+ *   out_f32   device fp32 [batch*seq][d_model] = Y
+ */
+tp_status tp_block_forward(tp_plan_t plan, const void* x, int batch, int seq, int causal,
+                           void* k_cache, void* v_cache, int cache_cap, int cache_pos,
+                           const void* packed, void* workspace, size_t ws_bytes,
+                           void* out_f32, void* stream);
+
+/*
+ * Wait for `stream`, then report (and clear) the first device-side error
+ * recorded by a bounded wait in this library's kernels on the current
+ * device: TP_ERR_DEVICE_TIMEOUT, TP_ERR_CUDA on a CUDA error, else TP_OK.
+ */
+tp_status tp_sync_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H_ */

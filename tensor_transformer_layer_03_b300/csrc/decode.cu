@@ -1,0 +1,146 @@
+// Single-token decode attention over the per-head KV cache.
+//
+// Each head's cache rows belong to the shard that owns the head ("Tensor
+// Parallelism: Splitting One Layer Across GPUs" (byteledger), "Interaction
+// with the rest of serving"), so a (sequence, head) pair is independent work.
+// One query row per head leaves too little parallelism for one block per
+// head, so the keys are split into chunks: pass 1 computes, per chunk, the
+// running max m, the sum l of exp(s - m) and the unnormalised output
+// sum_j exp(s_j - m) v_j; pass 2 merges the chunks with the usual
+// log-sum-exp rescaling and writes softmax(q K^T / sqrt(d_head)) V.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tpk {
+
+namespace {
+
+constexpr int DEC_THREADS = 128;  // keys scored per sub-chunk (one per thread)
+
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+    const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < DEC_THREADS / 32; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+    return r;
+}
+
+template <typename T, int DH>
+__global__ void __launch_bounds__(DEC_THREADS) decode_split_k(AttnArgs a, float* __restrict__ part, int chunk,
+                                                              int nsplit) {
+    constexpr int G = DEC_THREADS / DH;  // key groups in the P.V pass
+    __shared__ float qs[DH];
+    __shared__ float ps[DEC_THREADS];
+    __shared__ float red[DEC_THREADS / 32];
+    __shared__ float ored[G][DH];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int s = h / a.hl, jl = h % a.hl;
+    const long long M = (long long)a.B;  // one query token per sequence
+    const T* q = (const T*)a.qkv + ((long long)s * M + b) * (3 * a.hl * DH) + jl * DH;
+    for (int i = threadIdx.x; i < DH; i += DEC_THREADS) qs[i] = to_f(q[i]) * a.scale;
+    const int L = a.pos + 1;
+    const int k0 = c * chunk, k1 = min(L, k0 + chunk);
+    const T* kbase = (const T*)a.kc + ((long long)b * a.H + h) * a.cap * DH;
+    const T* vbase = (const T*)a.vc + ((long long)b * a.H + h) * a.cap * DH;
+    const int dim = threadIdx.x % DH, grp = threadIdx.x / DH;
+    float m_run = -INFINITY, l_run = 0.f, o_acc = 0.f;
+    __syncthreads();
+    for (int sub = k0; sub < k1; sub += DEC_THREADS) {
+        const int key = sub + threadIdx.x;
+        float sc = -INFINITY;
+        if (key < k1) {
+            const T* kr = kbase + (long long)key * DH;
+            float dot = 0.f;
+#pragma unroll 16
+            for (int i = 0; i < DH; ++i) dot = fmaf(qs[i], to_f(kr[i]), dot);
+            sc = dot;
+        }
+        const float mt = block_reduce(sc, red, true);
+        const float mnew = fmaxf(m_run, mt);
+        const float p = key < k1 ? expf(sc - mnew) : 0.f;
+        ps[threadIdx.x] = p;
+        const float lt = block_reduce(p, red, false);  // also orders the ps writes
+        const float corr = m_run == -INFINITY ? 0.f : expf(m_run - mnew);
+        l_run = l_run * corr + lt;
+        o_acc *= corr;
+        const int nk = min(DEC_THREADS, k1 - sub);
+        for (int j = grp; j < nk; j += G) o_acc = fmaf(ps[j], to_f(vbase[(long long)(sub + j) * DH + dim]), o_acc);
+        m_run = mnew;
+        __syncthreads();
+    }
+    ored[grp][dim] = o_acc;
+    __syncthreads();
+    float* dst = part + (((long long)b * a.H + h) * DECODE_MAX_SPLITS + c) * (DH + 2);
+    if (threadIdx.x < DH) {
+        float o = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) o += ored[g2][threadIdx.x];
+        dst[2 + threadIdx.x] = o;
+    }
+    if (threadIdx.x == 0) {
+        dst[0] = m_run;
+        dst[1] = l_run;
+    }
+}
+
+template <typename T, int DH>
+__global__ void __launch_bounds__(DH) decode_combine_k(AttnArgs a, const float* __restrict__ part, int nsplit) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int s = h / a.hl, jl = h % a.hl;
+    const float* src = part + ((long long)b * a.H + h) * DECODE_MAX_SPLITS * (DH + 2);
+    float mx = -INFINITY;
+    for (int c = 0; c < nsplit; ++c) mx = fmaxf(mx, src[c * (DH + 2)]);
+    float l = 0.f, o = 0.f;
+    for (int c = 0; c < nsplit; ++c) {
+        const float* pc = src + c * (DH + 2);
+        const float w = expf(pc[0] - mx);
+        l = fmaf(pc[1], w, l);
+        o = fmaf(pc[2 + threadIdx.x], w, o);
+    }
+    T* out = (T*)a.out + ((long long)s * a.B + b) * (a.hl * DH) + jl * DH;
+    out[threadIdx.x] = from_f<T>(o / l);
+}
+
+template <typename T, int DH>
+cudaError_t decode_launch(const AttnArgs& a, float* scratch, cudaStream_t st) {
+    const int L = a.pos + 1;
+    int nsplit = (L + DEC_THREADS - 1) / DEC_THREADS;
+    int chunk = DEC_THREADS;
+    if (nsplit > DECODE_MAX_SPLITS) {
+        chunk = ((L + DECODE_MAX_SPLITS - 1) / DECODE_MAX_SPLITS + DEC_THREADS - 1) / DEC_THREADS * DEC_THREADS;
+        nsplit = (L + chunk - 1) / chunk;
+    }
+    decode_split_k<T, DH><<<dim3(nsplit, a.H, a.B), DEC_THREADS, 0, st>>>(a, scratch, chunk, nsplit);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_k<T, DH><<<dim3(a.H, a.B), DH, 0, st>>>(a, scratch, nsplit);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t decode_t(const AttnArgs& a, float* scratch, cudaStream_t st) {
+    switch (a.dh) {
+        case 32: return decode_launch<T, 32>(a, scratch, st);
+        case 64: return decode_launch<T, 64>(a, scratch, st);
+        case 128: return decode_launch<T, 128>(a, scratch, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t decode_attention(const AttnArgs& a, float* scratch, cudaStream_t st) {
+    return a.is_bf16 ? decode_t<bf16>(a, scratch, st) : decode_t<float>(a, scratch, st);
+}
+
+}  // namespace tpk

@@ -1,0 +1,91 @@
+// Internal launch interface between the C ABI (tp_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tpk {
+
+// ---- weight packing (pack.cu) ----------------------------------------------
+// dst[s][r][c], r < 3*hl*dh: rows of Wq/Wk/Wv belonging to shard s's heads.
+cudaError_t pack_qkv(int esize, const void* Wq, const void* Wk, const void* Wv, void* dst, int tp, int hl,
+                     int dh, int d, cudaStream_t st);
+// dst[s][n][k] = src[n][s*ks + k]   (src is [N][tp*ks])
+cudaError_t pack_cols(int esize, const void* src, void* dst, int tp, int N, int ks, cudaStream_t st);
+// SwiGLU: dst[s][r][c] with `granule`-row blocks alternating gate/up of shard s.
+// GELU (Wu == nullptr): dst[s][r][c] = W1[s*fl + r][c].
+cudaError_t pack_up(int esize, const void* Wg, const void* Wu, void* dst, int tp, int fl, int d, int granule,
+                    cudaStream_t st);
+
+// ---- SIMT path (simt.cu): fp32 plans, and shapes the tensor-core path does not take
+enum SimtEpi { EPI_STORE = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_ROW_REDUCE = 3 };
+
+struct SimtGemm {
+    int epi;
+    int is_bf16;
+    const void* A;        // [.., M, lda]
+    long long a_shard;    // elements between shards of A (0: shared input)
+    int lda;
+    const void* W;        // [.., N, ldw]
+    long long w_shard;
+    int ldw;
+    int M, N, K;          // N = W rows per shard, K = reduction length per shard
+    int col_shards;       // grid.z: shards computed side by side (column)
+    int red_shards;       // shards summed into one output (row reduce)
+    void* out;            // column: act [cs][M][ldo]; row: fp32 [M][ldo]
+    long long out_shard;
+    int ldo;
+    void* out2;           // row: optional act copy
+    const void* residual; // row: optional
+    int residual_f32;
+    int granule;          // SwiGLU: gate/up interleave block (rows)
+};
+cudaError_t simt_gemm(const SimtGemm& g, cudaStream_t st);
+
+struct AttnArgs {
+    int is_bf16;
+    const void* qkv;      // [tp][B*Tq][3*hl*dh]
+    const void* kc;       // cache [B][H][cap][dh] or nullptr
+    const void* vc;
+    void* out;            // [tp][B*Tq][hl*dh]
+    int B, Tq, H, hl, dh, cap, pos, causal;
+    float scale;
+};
+// K/V of the new tokens -> cache positions pos..pos+Tq-1
+cudaError_t kv_append(const AttnArgs& a, void* kc, void* vc, cudaStream_t st);
+cudaError_t simt_attention(const AttnArgs& a, cudaStream_t st);
+
+// ---- tensor-core GEMM (gemm_tc.cu): bf16 in, fp32 accumulate in TMEM -------
+struct TcGemm {
+    int epi;              // EPI_STORE / EPI_GELU / EPI_SWIGLU / EPI_ROW_REDUCE
+    const void* A;        // bf16 [shards?][M][lda]
+    long long a_shard;    // elements between A shards (0 for column-parallel)
+    int lda;
+    const void* W;        // bf16 [shards][N][K]
+    long long w_shard;
+    int M, N, K;          // per shard: N = W rows, K = reduction length
+    int shards;
+    int reduce;           // 1: sum all shards into one output (row-parallel)
+    void* out;
+    long long out_shard;
+    int ldo;
+    int granule;
+    void* out2;
+    const void* residual;
+    int residual_f32;
+};
+bool tc_gemm_supported(int M, int N, int K);
+cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st);
+
+// ---- tensor-core attention (attn_tc.cu) --------------------------------------
+bool tc_attention_supported(const AttnArgs& a);
+cudaError_t tc_attention(const AttnArgs& a, cudaStream_t st);
+
+// ---- single-token decode (decode.cu) ------------------------------------------
+// Split-KV attention: partial (max, sum, output) per key chunk in `scratch`
+// ([B][H][DECODE_MAX_SPLITS][dh + 2] floats), then a combine pass.
+constexpr int DECODE_MAX_SPLITS = 64;
+cudaError_t decode_attention(const AttnArgs& a, float* scratch, cudaStream_t st);
+
+}  // namespace tpk

@@ -1,0 +1,378 @@
+// C ABI of the tensor-parallel block: plan, validation, layout and dispatch.
+//
+// Everything here runs on the host.  Calls validate their arguments before
+// enqueuing anything, then launch the kernels of pack.cu, simt.cu,
+// gemm_tc.cu, attn_tc.cu and decode.cu on the caller's stream.
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "kernels.h"
+#include "tp.h"
+
+// First device-side error recorded by a bounded wait (0 = none).  Kernels
+// receive its address; tp_sync_status reads and clears it.
+__device__ int g_tp_device_error;
+
+struct tp_plan_s {
+    int d, H, dh, f, tp, hl, fl, granule, up_rows;
+    tp_act act;
+    tp_dtype dtype;
+    int esize;
+    size_t off_qkv, off_o, off_up, off_down, packed_bytes;
+};
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+tp_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return TP_OK;
+    strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
+    return TP_ERR_CUDA;
+}
+
+int* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static int* addr[64] = {nullptr};
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_tp_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int*>(p);
+    }
+    return addr[dev];
+}
+
+struct Workspace {
+    size_t qkv, attn, hf32, hact, u, scratch, total;
+};
+
+size_t attn_scratch_bytes(const tp_plan_s* p, int batch, int seq_q) {
+    if (seq_q != 1) return 0;
+    return align_up((size_t)batch * p->H * tpk::DECODE_MAX_SPLITS * (p->dh + 2) * sizeof(float), 256);
+}
+
+Workspace workspace_layout(const tp_plan_s* p, int batch, int seq) {
+    const size_t M = (size_t)batch * seq, es = p->esize;
+    Workspace w;
+    size_t o = 0;
+    w.qkv = o;   o = align_up(o + (size_t)p->tp * M * 3 * p->hl * p->dh * es, 1024);
+    w.attn = o;  o = align_up(o + (size_t)p->tp * M * p->hl * p->dh * es, 1024);
+    w.hf32 = o;  o = align_up(o + M * p->d * sizeof(float), 1024);
+    w.hact = o;  o = align_up(o + M * p->d * es, 1024);
+    w.u = o;     o = align_up(o + (size_t)p->tp * M * p->fl * es, 1024);
+    w.scratch = o; o = align_up(o + attn_scratch_bytes(p, batch, seq), 1024);
+    w.total = o;
+    return w;
+}
+
+const char* ptr_at(const void* base, size_t off) { return static_cast<const char*>(base) + off; }
+char* ptr_at(void* base, size_t off) { return static_cast<char*>(base) + off; }
+
+}  // namespace
+
+extern "C" {
+
+const char* tp_status_string(tp_status s) {
+    switch (s) {
+        case TP_OK: return "TP_OK";
+        case TP_ERR_NULL_ARG: return "TP_ERR_NULL_ARG";
+        case TP_ERR_INVALID_DIM: return "TP_ERR_INVALID_DIM";
+        case TP_ERR_DEGREE_RANGE: return "TP_ERR_DEGREE_RANGE";
+        case TP_ERR_HEADS_NOT_DIVISIBLE: return "TP_ERR_HEADS_NOT_DIVISIBLE";
+        case TP_ERR_FFN_NOT_DIVISIBLE: return "TP_ERR_FFN_NOT_DIVISIBLE";
+        case TP_ERR_DMODEL_NOT_DIVISIBLE: return "TP_ERR_DMODEL_NOT_DIVISIBLE";
+        case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT";
+        case TP_ERR_WORKSPACE_TOO_SMALL: return "TP_ERR_WORKSPACE_TOO_SMALL";
+        case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+        case TP_ERR_CUDA: return "TP_ERR_CUDA";
+        case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT";
+    }
+    return "TP_ERR_UNKNOWN";
+}
+
+const char* tp_last_cuda_error(void) { return g_last_cuda_error; }
+
+tp_status tp_plan_create_ex(int d_model, int n_heads, int d_ffn, int tp_degree, tp_act act, tp_dtype dtype,
+                            tp_plan_t* out) {
+    if (!out) return TP_ERR_NULL_ARG;
+    *out = nullptr;
+    if (d_model <= 0 || n_heads <= 0 || d_ffn <= 0) return TP_ERR_INVALID_DIM;
+    if (tp_degree < 1) return TP_ERR_DEGREE_RANGE;
+    if (d_model % n_heads != 0) return TP_ERR_DMODEL_NOT_DIVISIBLE;
+    if (tp_degree > n_heads) return TP_ERR_DEGREE_RANGE;
+    if (n_heads % tp_degree != 0) return TP_ERR_HEADS_NOT_DIVISIBLE;
+    if (d_ffn % tp_degree != 0) return TP_ERR_FFN_NOT_DIVISIBLE;
+    if ((act != TP_ACT_GELU && act != TP_ACT_SWIGLU) || (dtype != TP_BF16 && dtype != TP_FP32))
+        return TP_ERR_UNSUPPORTED;
+    const int dh = d_model / n_heads, fl = d_ffn / tp_degree;
+    if (d_model % 8 || dh % 8 || fl % 8) return TP_ERR_ALIGNMENT;
+
+    tp_plan_s* p = new (std::nothrow) tp_plan_s;
+    if (!p) return TP_ERR_UNSUPPORTED;
+    p->d = d_model;
+    p->H = n_heads;
+    p->dh = dh;
+    p->f = d_ffn;
+    p->tp = tp_degree;
+    p->hl = n_heads / tp_degree;
+    p->fl = fl;
+    p->granule = fl % 32 == 0 ? 32 : (fl % 16 == 0 ? 16 : 8);
+    p->act = act;
+    p->dtype = dtype;
+    p->esize = dtype == TP_BF16 ? 2 : 4;
+    p->up_rows = act == TP_ACT_SWIGLU ? 2 * fl : fl;
+    const size_t es = p->esize, d = d_model, T = tp_degree;
+    size_t o = 0;
+    p->off_qkv = o;  o = align_up(o + T * 3 * p->hl * dh * d * es, 1024);
+    p->off_o = o;    o = align_up(o + T * d * p->hl * dh * es, 1024);
+    p->off_up = o;   o = align_up(o + T * p->up_rows * d * es, 1024);
+    p->off_down = o; o = align_up(o + T * d * fl * es, 1024);
+    p->packed_bytes = o;
+    *out = p;
+    return TP_OK;
+}
+
+tp_status tp_plan_create(int d_model, int n_heads, int d_ffn, int tp_degree, tp_plan_t* out) {
+    return tp_plan_create_ex(d_model, n_heads, d_ffn, tp_degree, TP_ACT_SWIGLU, TP_BF16, out);
+}
+
+void tp_plan_destroy(tp_plan_t plan) { delete plan; }
+
+tp_status tp_plan_sizes(tp_plan_t p, int batch, int seq, size_t* packed_weight_bytes, size_t* workspace_bytes) {
+    if (!p) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
+    if (packed_weight_bytes) *packed_weight_bytes = p->packed_bytes;
+    if (workspace_bytes) *workspace_bytes = workspace_layout(p, batch, seq).total;
+    return TP_OK;
+}
+
+tp_status tp_attention_scratch_bytes(tp_plan_t p, int batch, int seq_q, int cache_cap, size_t* bytes) {
+    if (!p || !bytes) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq_q <= 0 || cache_cap < 0) return TP_ERR_INVALID_DIM;
+    *bytes = attn_scratch_bytes(p, batch, seq_q);
+    return TP_OK;
+}
+
+tp_status tp_shard_weights(tp_plan_t p, const void* Wq, const void* Wk, const void* Wv, const void* Wo,
+                           const void* W1_or_Wgate, const void* Wup, const void* Wdown, void* packed,
+                           void* stream) {
+    if (!p || !Wq || !Wk || !Wv || !Wo || !W1_or_Wgate || !Wdown || !packed) return TP_ERR_NULL_ARG;
+    if ((p->act == TP_ACT_SWIGLU) != (Wup != nullptr)) return TP_ERR_NULL_ARG;
+    const void* all[] = {Wq, Wk, Wv, Wo, W1_or_Wgate, Wup, Wdown, packed};
+    for (const void* q : all)
+        if (misaligned(q)) return TP_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int es = p->esize;
+    cudaError_t e = tpk::pack_qkv(es, Wq, Wk, Wv, ptr_at(packed, p->off_qkv), p->tp, p->hl, p->dh, p->d, st);
+    if (e == cudaSuccess) e = tpk::pack_cols(es, Wo, ptr_at(packed, p->off_o), p->tp, p->d, p->hl * p->dh, st);
+    if (e == cudaSuccess)
+        e = tpk::pack_up(es, W1_or_Wgate, Wup, ptr_at(packed, p->off_up), p->tp, p->fl, p->d, p->granule, st);
+    if (e == cudaSuccess) e = tpk::pack_cols(es, Wdown, ptr_at(packed, p->off_down), p->tp, p->d, p->fl, st);
+    return cuda_status(e);
+}
+
+tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const void* packed, void* out_shards,
+                           void* stream) {
+    if (!p || !x || !packed || !out_shards) return TP_ERR_NULL_ARG;
+    if (M <= 0 || (which != TP_QKV && which != TP_FFN_UP)) return TP_ERR_INVALID_DIM;
+    if (misaligned(x) || misaligned(packed) || misaligned(out_shards)) return TP_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool qkv = which == TP_QKV;
+    const int N = qkv ? 3 * p->hl * p->dh : p->up_rows;  // W rows per shard
+    const int n_out = qkv ? N : p->fl;                     // output columns per shard
+    const void* W = ptr_at(packed, qkv ? p->off_qkv : p->off_up);
+    const int epi = qkv ? tpk::EPI_STORE : (p->act == TP_ACT_SWIGLU ? tpk::EPI_SWIGLU : tpk::EPI_GELU);
+    if (p->dtype == TP_BF16 && tpk::tc_gemm_supported(M, N, p->d)) {
+        tpk::TcGemm g{};
+        g.epi = epi;
+        g.A = x;
+        g.a_shard = 0;
+        g.lda = p->d;
+        g.W = W;
+        g.w_shard = (long long)N * p->d;
+        g.M = M;
+        g.N = N;
+        g.K = p->d;
+        g.shards = p->tp;
+        g.reduce = 0;
+        g.out = out_shards;
+        g.out_shard = (long long)M * n_out;
+        g.ldo = n_out;
+        g.granule = p->granule;
+        return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
+    }
+    tpk::SimtGemm g{};
+    g.epi = epi;
+    g.is_bf16 = p->dtype == TP_BF16;
+    g.A = x;
+    g.a_shard = 0;
+    g.lda = p->d;
+    g.W = W;
+    g.w_shard = (long long)N * p->d;
+    g.ldw = p->d;
+    g.M = M;
+    g.N = N;
+    g.K = p->d;
+    g.col_shards = p->tp;
+    g.red_shards = 1;
+    g.out = out_shards;
+    g.out_shard = (long long)M * n_out;
+    g.ldo = n_out;
+    g.granule = p->granule;
+    return cuda_status(tpk::simt_gemm(g, st));
+}
+
+tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
+                               const void* residual, void* out_f32, void* out_act, void* stream) {
+    if (!p || !in_shards || !packed || !out_f32) return TP_ERR_NULL_ARG;
+    if (M <= 0 || (which != TP_ATTN_OUT && which != TP_FFN_DOWN)) return TP_ERR_INVALID_DIM;
+    if (misaligned(in_shards) || misaligned(packed) || misaligned(residual) || misaligned(out_f32) ||
+        misaligned(out_act))
+        return TP_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool attn = which == TP_ATTN_OUT;
+    const int ks = attn ? p->hl * p->dh : p->fl;
+    const void* W = ptr_at(packed, attn ? p->off_o : p->off_down);
+    const int res_f32 = attn ? (p->dtype == TP_FP32) : 1;
+    if (p->dtype == TP_BF16 && tpk::tc_gemm_supported(M, p->d, ks)) {
+        tpk::TcGemm g{};
+        g.epi = tpk::EPI_ROW_REDUCE;
+        g.A = in_shards;
+        g.a_shard = (long long)M * ks;
+        g.lda = ks;
+        g.W = W;
+        g.w_shard = (long long)p->d * ks;
+        g.M = M;
+        g.N = p->d;
+        g.K = ks;
+        g.shards = p->tp;
+        g.reduce = 1;
+        g.out = out_f32;
+        g.ldo = p->d;
+        g.out2 = out_act;
+        g.residual = residual;
+        g.residual_f32 = res_f32;
+        return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
+    }
+    tpk::SimtGemm g{};
+    g.epi = tpk::EPI_ROW_REDUCE;
+    g.is_bf16 = p->dtype == TP_BF16;
+    g.A = in_shards;
+    g.a_shard = (long long)M * ks;
+    g.lda = ks;
+    g.W = W;
+    g.w_shard = (long long)p->d * ks;
+    g.ldw = ks;
+    g.M = M;
+    g.N = p->d;
+    g.K = ks;
+    g.col_shards = 1;
+    g.red_shards = p->tp;
+    g.out = out_f32;
+    g.ldo = p->d;
+    g.out2 = out_act;
+    g.residual = residual;
+    g.residual_f32 = res_f32;
+    return cuda_status(tpk::simt_gemm(g, st));
+}
+
+tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int seq_q, int causal, void* k_cache,
+                             void* v_cache, int cache_cap, int cache_pos, void* out_shards, void* scratch,
+                             size_t scratch_bytes, void* stream) {
+    if (!p || !qkv_shards || !out_shards) return TP_ERR_NULL_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq_q <= 0 || cache_pos < 0) return TP_ERR_INVALID_DIM;
+    const bool cached = k_cache != nullptr;
+    if (!cached && cache_pos != 0) return TP_ERR_INVALID_DIM;
+    if (cached && (cache_cap <= 0 || (long long)cache_pos + seq_q > cache_cap)) return TP_ERR_INVALID_DIM;
+    if (misaligned(qkv_shards) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out_shards) ||
+        misaligned(scratch))
+        return TP_ERR_ALIGNMENT;
+    if (p->dh != 32 && p->dh != 64 && p->dh != 128) return TP_ERR_UNSUPPORTED;
+    const size_t need = cached ? attn_scratch_bytes(p, batch, seq_q) : 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    tpk::AttnArgs a{};
+    a.is_bf16 = p->dtype == TP_BF16;
+    a.qkv = qkv_shards;
+    a.kc = k_cache;
+    a.vc = v_cache;
+    a.out = out_shards;
+    a.B = batch;
+    a.Tq = seq_q;
+    a.H = p->H;
+    a.hl = p->hl;
+    a.dh = p->dh;
+    a.cap = cached ? cache_cap : 0;
+    a.pos = cache_pos;
+    a.causal = causal ? 1 : 0;
+    a.scale = 1.0f / sqrtf((float)p->dh);
+    const bool split_kv = cached && seq_q == 1 && need > 0;
+    if (split_kv && !scratch) return TP_ERR_NULL_ARG;
+    if (split_kv && scratch_bytes < need) return TP_ERR_WORKSPACE_TOO_SMALL;
+    cudaError_t e = cudaSuccess;
+    if (cached) {
+        e = tpk::kv_append(a, k_cache, v_cache, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    if (split_kv) {
+        e = tpk::decode_attention(a, static_cast<float*>(scratch), st);
+    } else if (a.is_bf16 && tpk::tc_attention_supported(a)) {
+        e = tpk::tc_attention(a, st);
+    } else {
+        e = tpk::simt_attention(a, st);
+    }
+    return cuda_status(e);
+}
+
+tp_status tp_block_forward(tp_plan_t p, const void* x, int batch, int seq, int causal, void* k_cache,
+                           void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
+                           size_t ws_bytes, void* out_f32, void* stream) {
+    if (!p || !x || !packed || !workspace || !out_f32) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
+    if (misaligned(workspace)) return TP_ERR_ALIGNMENT;
+    const Workspace w = workspace_layout(p, batch, seq);
+    if (ws_bytes < w.total) return TP_ERR_WORKSPACE_TOO_SMALL;
+    const int M = batch * seq;
+    void* qkv = ptr_at(workspace, w.qkv);
+    void* attn = ptr_at(workspace, w.attn);
+    void* hf32 = ptr_at(workspace, w.hf32);
+    void* hact = ptr_at(workspace, w.hact);
+    void* u = ptr_at(workspace, w.u);
+    tp_status s = tp_column_linear(p, TP_QKV, x, M, packed, qkv, stream);
+    if (s != TP_OK) return s;
+    s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
+                           ptr_at(workspace, w.scratch), w.total - w.scratch, stream);
+    if (s != TP_OK) return s;
+    s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, stream);
+    if (s != TP_OK) return s;
+    s = tp_column_linear(p, TP_FFN_UP, hact, M, packed, u, stream);
+    if (s != TP_OK) return s;
+    return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, nullptr, stream);
+}
+
+tp_status tp_sync_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    int* word = device_error_word();
+    if (!word) return cuda_status(cudaGetLastError());
+    int h = 0;
+    e = cudaMemcpy(&h, word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (h != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_status(e);
+        return TP_ERR_DEVICE_TIMEOUT;
+    }
+    return TP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+"""Device-side driver of the library: torch allocates, ``libtp.so`` computes.
+
+``TPBlock`` holds one plan, the packed weights and a workspace on a CUDA
+device and runs the block through the C ABI.  Torch is used only for device
+memory, copies and streams.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import tp as _tp
+
+
+def _dev_bytes(nbytes: int, device) -> torch.Tensor:
+    # 16-byte aligned by the caching allocator (512-byte granularity)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+class TPBlock:
+    """One tensor-parallel block with its weights resident on ``device``."""
+
+    def __init__(self, shape, tp_degree: int, dtype: str, weights: dict, device="cuda",
+                 max_batch: int = 1, max_seq: int = 1, stream=None):
+        self.shape, self.tp, self.dtype, self.device = shape, tp_degree, dtype, torch.device(device)
+        self.plan = _tp.Plan(shape.d_model, shape.n_heads, shape.d_ffn, tp_degree, act=shape.act, dtype=dtype)
+        packed_bytes, _ = self.plan.sizes(1, 1)
+        self.packed = _dev_bytes(packed_bytes, self.device)
+        dev_w = {k: v.to(self.device, non_blocking=False).contiguous() for k, v in weights.items()}
+        self.plan.shard_weights(dev_w, self.packed, stream)
+        torch.cuda.synchronize(self.device)
+        del dev_w
+        self.workspace = None
+        self.reserve(max_batch, max_seq)
+
+    def reserve(self, batch: int, seq: int):
+        _, ws = self.plan.sizes(batch, seq)
+        if self.workspace is None or self.workspace.numel() < ws:
+            self.workspace = _dev_bytes(ws, self.device)
+
+    def forward(self, x: torch.Tensor, causal: bool, out: torch.Tensor | None = None, k_cache=None, v_cache=None,
+                cache_pos: int = 0, stream=None) -> torch.Tensor:
+        """x: device [B, T, d] in the plan dtype.  Returns Y fp32 [B, T, d]."""
+        B, T, d = x.shape
+        self.reserve(B, T)
+        if out is None:
+            out = torch.empty(B, T, d, dtype=torch.float32, device=self.device)
+        cap = 0 if k_cache is None else k_cache.shape[2]
+        self.plan.block_forward(x, B, T, causal, self.packed, self.workspace, out, k_cache, v_cache, cap, cache_pos,
+                                stream)
+        return out

@@ -1,0 +1,157 @@
+"""ctypes binding of ``libtp.so`` (declared in ``include/tp.h``).
+
+Argument marshalling only: every function keeps the C name and signature,
+and tensors are passed as raw device pointers (``tensor.data_ptr()``).  All
+work runs in the library's CUDA kernels; there is no Python or CPU
+fallback -- if the library is missing, importing this module raises.
+
+``Plan`` is a small convenience wrapper that owns a ``tp_plan_t`` and takes
+torch tensors; it only converts arguments and checks status codes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtp.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run `python -m tensor_transformer_layer_03_b300.build` "
+                      "(or __graft_entry__.build()) first")
+lib = ctypes.CDLL(LIB_PATH)
+
+# ---- enums (same values as include/tp.h) ------------------------------------
+TP_OK = 0
+STATUS_NAMES = ("OK", "NULL_ARG", "INVALID_DIM", "DEGREE_RANGE", "HEADS_NOT_DIVISIBLE", "FFN_NOT_DIVISIBLE",
+                "DMODEL_NOT_DIVISIBLE", "ALIGNMENT", "WORKSPACE_TOO_SMALL", "UNSUPPORTED", "CUDA",
+                "DEVICE_TIMEOUT")
+TP_ACT_GELU, TP_ACT_SWIGLU = 0, 1
+TP_BF16, TP_FP32 = 0, 1
+TP_QKV, TP_FFN_UP = 0, 1
+TP_ATTN_OUT, TP_FFN_DOWN = 0, 1
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_plan_p = ctypes.POINTER(ctypes.c_void_p)
+
+EXPORTS = {
+    "tp_status_string": (ctypes.c_char_p, [_i]),
+    "tp_last_cuda_error": (ctypes.c_char_p, []),
+    "tp_plan_create": (_i, [_i, _i, _i, _i, _plan_p]),
+    "tp_plan_create_ex": (_i, [_i, _i, _i, _i, _i, _i, _plan_p]),
+    "tp_plan_destroy": (None, [_p]),
+    "tp_plan_sizes": (_i, [_p, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
+    "tp_attention_scratch_bytes": (_i, [_p, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "tp_shard_weights": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "tp_column_linear": (_i, [_p, _i, _p, _i, _p, _p, _p]),
+    "tp_row_linear_reduce": (_i, [_p, _i, _p, _i, _p, _p, _p, _p, _p]),
+    "tp_attention_heads": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p]),
+    "tp_block_forward": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p, _p]),
+    "tp_sync_status": (_i, [_p]),
+}
+for _name, (_res, _args) in EXPORTS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+    globals()[_name] = _f
+
+
+class TPError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        self.name = STATUS_NAMES[code] if 0 <= code < len(STATUS_NAMES) else f"UNKNOWN({code})"
+        msg = f"{where}: TP_ERR_{self.name}" if code else where
+        if self.name == "CUDA":
+            msg += f" ({tp_last_cuda_error().decode()})"
+        super().__init__(msg)
+
+
+def check(code: int, where: str = "") -> None:
+    if code != TP_OK:
+        raise TPError(code, where)
+
+
+def status_name(code: int) -> str:
+    return STATUS_NAMES[code]
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """Owns a tp_plan_t.  Methods take torch tensors (device pointers)."""
+
+    def __init__(self, d_model, n_heads, d_ffn, tp_degree, act="swiglu", dtype="bf16"):
+        h = ctypes.c_void_p()
+        code = tp_plan_create_ex(d_model, n_heads, d_ffn, tp_degree,
+                                 TP_ACT_SWIGLU if act == "swiglu" else TP_ACT_GELU,
+                                 TP_BF16 if dtype == "bf16" else TP_FP32, ctypes.byref(h))
+        check(code, "tp_plan_create_ex")
+        self.handle = h
+        self.d_model, self.n_heads, self.d_ffn, self.tp = d_model, n_heads, d_ffn, tp_degree
+        self.d_head = d_model // n_heads
+        self.h_l, self.f_l = n_heads // tp_degree, d_ffn // tp_degree
+        self.act, self.dtype = act, dtype
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            tp_plan_destroy(h)
+            self.handle = None
+
+    def sizes(self, batch, seq):
+        pw, ws = _sz(), _sz()
+        check(tp_plan_sizes(self.handle, batch, seq, ctypes.byref(pw), ctypes.byref(ws)), "tp_plan_sizes")
+        return pw.value, ws.value
+
+    def attention_scratch_bytes(self, batch, seq_q, cache_cap):
+        b = _sz()
+        check(tp_attention_scratch_bytes(self.handle, batch, seq_q, cache_cap, ctypes.byref(b)),
+              "tp_attention_scratch_bytes")
+        return b.value
+
+    def shard_weights(self, w: dict, packed, stream=None):
+        up = w.get("Wu")
+        first = w["Wg"] if up is not None else w["W1"]
+        check(tp_shard_weights(self.handle, _ptr(w["Wq"]), _ptr(w["Wk"]), _ptr(w["Wv"]), _ptr(w["Wo"]),
+                               _ptr(first), _ptr(up), _ptr(w["Wd"]), _ptr(packed), _stream(stream)),
+              "tp_shard_weights")
+
+    def column_linear(self, which, x, M, packed, out, stream=None):
+        check(tp_column_linear(self.handle, which, _ptr(x), M, _ptr(packed), _ptr(out), _stream(stream)),
+              "tp_column_linear")
+
+    def row_linear_reduce(self, which, inp, M, packed, residual, out_f32, out_act=None, stream=None):
+        check(tp_row_linear_reduce(self.handle, which, _ptr(inp), M, _ptr(packed), _ptr(residual),
+                                   _ptr(out_f32), _ptr(out_act), _stream(stream)), "tp_row_linear_reduce")
+
+    def attention_heads(self, qkv, batch, seq_q, causal, k_cache, v_cache, cache_cap, cache_pos, out,
+                        scratch=None, stream=None):
+        nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+        check(tp_attention_heads(self.handle, _ptr(qkv), batch, seq_q, int(causal), _ptr(k_cache), _ptr(v_cache),
+                                 cache_cap, cache_pos, _ptr(out), _ptr(scratch), nbytes, _stream(stream)),
+              "tp_attention_heads")
+
+    def block_forward(self, x, batch, seq, causal, packed, workspace, out_f32, k_cache=None, v_cache=None,
+                      cache_cap=0, cache_pos=0, stream=None):
+        nbytes = workspace.numel() * workspace.element_size()
+        check(tp_block_forward(self.handle, _ptr(x), batch, seq, int(causal), _ptr(k_cache), _ptr(v_cache),
+                               cache_cap, cache_pos, _ptr(packed), _ptr(workspace), nbytes, _ptr(out_f32),
+                               _stream(stream)), "tp_block_forward")
+
+    def sync_status(self, stream=None):
+        check(tp_sync_status(_stream(stream)), "tp_sync_status")

@@ -1,0 +1,153 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, and
+its host-side plan logic and argument validation behave as documented.
+No call here reaches a kernel launch (validation fails first)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import oracle.tp_oracle as o
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import __graft_entry__
+    __graft_entry__.build()
+    from tensor_transformer_layer_03_b300 import tp as binding
+    return binding
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(tp_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(tp):
+    names = declared_functions()
+    assert "tp_block_forward" in names and "tp_plan_create" in names
+    for n in names:
+        assert hasattr(tp.lib, n), f"{n} declared in include/ but not exported"
+        assert n in tp.EXPORTS, f"{n} has no binding"
+
+
+def _create(tp, d, H, f, deg, act=1, dtype=0):
+    h = ctypes.c_void_p()
+    code = tp.tp_plan_create_ex(d, H, f, deg, act, dtype, ctypes.byref(h))
+    return code, h
+
+
+def test_plan_rules_match_golden_and_oracle(tp):
+    table = json.load(open(os.path.join(ROOT, "tests", "golden", "plan_rules.json")))
+    for c in table["cases"]:
+        code, h = _create(tp, c["d_model"], c["n_heads"], c["d_ffn"], c["tp"])
+        assert tp.status_name(code) == c["expect"] == o.check_plan(c["d_model"], c["n_heads"], c["d_ffn"], c["tp"]), c
+        if code == 0:
+            assert h.value
+            tp.tp_plan_destroy(h)
+        else:
+            assert not h.value  # *out left NULL on error
+
+
+def test_plan_rules_exhaustive_small(tp):
+    for d in (8, 16, 24, 48, 64):
+        for H in range(0, 9):
+            for f in (0, 8, 16, 24, 40, 64):
+                for deg in range(-1, 10):
+                    code, h = _create(tp, d, H, f, deg)
+                    exp = o.check_plan(d, H, f, deg)
+                    got = tp.status_name(code)
+                    if exp == "OK":
+                        # this build additionally needs 8-element rows
+                        dh, fl = d // H, f // deg
+                        exp = "OK" if (d % 8 == 0 and dh % 8 == 0 and fl % 8 == 0) else "ALIGNMENT"
+                    assert got == exp, (d, H, f, deg, got, exp)
+                    if h.value:
+                        tp.tp_plan_destroy(h)
+
+
+def test_tp_plan_create_defaults_and_null(tp):
+    assert tp.tp_plan_create(4096, 32, 11008, 4, None) == 1  # NULL out -> TP_ERR_NULL_ARG
+    h = ctypes.c_void_p()
+    assert tp.tp_plan_create(5120, 40, 13824, 3, ctypes.byref(h)) == 4  # HEADS_NOT_DIVISIBLE
+    assert tp.tp_plan_create(4096, 32, 11008, 4, ctypes.byref(h)) == 0
+    tp.tp_plan_destroy(h)
+    assert tp.tp_plan_create_ex(256, 4, 1024, 2, 7, 0, ctypes.byref(h)) == 9  # unknown activation
+
+
+def test_status_strings(tp):
+    for i, n in enumerate(tp.STATUS_NAMES):
+        assert tp.tp_status_string(i).decode() == ("TP_OK" if n == "OK" else "TP_ERR_" + n)
+
+
+def test_sizes(tp):
+    for (d, H, f, deg, act, dt) in ((4096, 32, 11008, 4, 1, 0), (256, 4, 1024, 2, 0, 1), (5120, 40, 13824, 8, 1, 0)):
+        code, h = _create(tp, d, H, f, deg, act, dt)
+        assert code == 0
+        pw, ws = ctypes.c_size_t(), ctypes.c_size_t()
+        assert tp.tp_plan_sizes(h, 2, 128, ctypes.byref(pw), ctypes.byref(ws)) == 0
+        es = 2 if dt == 0 else 4
+        n_weights = 4 * d * d + (3 if act == 1 else 2) * d * f
+        assert n_weights * es <= pw.value <= n_weights * es + 8 * 4096
+        M = 256
+        acts = M * (3 * d + d + (f if True else 0)) * es + M * d * (4 + es)
+        assert ws.value >= acts
+        assert tp.tp_plan_sizes(h, 0, 128, ctypes.byref(pw), None) == 2
+        assert tp.tp_plan_sizes(None, 1, 1, None, None) == 1
+        sb = ctypes.c_size_t()
+        assert tp.tp_attention_scratch_bytes(h, 1, 128, 0, ctypes.byref(sb)) == 0 and sb.value == 0
+        assert tp.tp_attention_scratch_bytes(h, 2, 1, 1025, ctypes.byref(sb)) == 0 and sb.value > 0
+        tp.tp_plan_destroy(h)
+
+
+def test_argument_validation_before_launch(tp):
+    code, h = _create(tp, 256, 4, 1024, 2)
+    assert code == 0
+    P = lambda v: ctypes.c_void_p(v)  # fake device addresses: never dereferenced
+    good, odd = P(0x10000), P(0x10008)
+    # column linear
+    assert tp.tp_column_linear(None, 0, good, 4, good, good, None) == 1
+    assert tp.tp_column_linear(h, 0, None, 4, good, good, None) == 1
+    assert tp.tp_column_linear(h, 0, good, 0, good, good, None) == 2
+    assert tp.tp_column_linear(h, 5, good, 4, good, good, None) == 2
+    assert tp.tp_column_linear(h, 0, odd, 4, good, good, None) == 7
+    # row reduce
+    assert tp.tp_row_linear_reduce(h, 0, good, 4, good, None, None, None, None) == 1
+    assert tp.tp_row_linear_reduce(h, 3, good, 4, good, None, good, None, None) == 2
+    assert tp.tp_row_linear_reduce(h, 1, good, 4, good, odd, good, None, None) == 7
+    # attention
+    A = tp.tp_attention_heads
+    assert A(h, good, 1, 4, 1, good, None, 8, 0, good, None, 0, None) == 1      # one-sided cache
+    assert A(h, good, 1, 4, 1, None, None, 0, 2, good, None, 0, None) == 2      # pos without cache
+    assert A(h, good, 1, 4, 1, good, good, 5, 2, good, None, 0, None) == 2      # 2 + 4 > cap 5
+    assert A(h, good, 0, 4, 1, None, None, 0, 0, good, None, 0, None) == 2
+    assert A(h, good, 1, 1, 1, good, good, 8, 3, good, None, 0, None) == 1      # decode needs scratch
+    assert A(h, good, 1, 1, 1, good, good, 8, 3, good, good, 16, None) == 8     # scratch too small
+    assert A(h, odd, 1, 4, 1, None, None, 0, 0, good, None, 0, None) == 7
+    # block
+    B = tp.tp_block_forward
+    assert B(h, good, 1, 4, 1, None, None, 0, 0, good, good, 64, good, None) == 8  # workspace too small
+    assert B(h, good, 1, 4, 1, None, None, 0, 0, good, None, 1 << 30, good, None) == 1
+    assert B(h, good, 1, 0, 1, None, None, 0, 0, good, good, 1 << 30, good, None) == 2
+    # shard weights: SwiGLU needs Wup
+    assert tp.tp_shard_weights(h, good, good, good, good, good, None, good, good, None) == 1
+    tp.tp_plan_destroy(h)
+    code, h = _create(tp, 256, 4, 1024, 2, act=0)
+    assert tp.tp_shard_weights(h, good, good, good, good, good, good, good, good, None) == 1  # GELU: no Wup
+    tp.tp_plan_destroy(h)
+
+
+def test_unsupported_head_width(tp):
+    code, h = _create(tp, 192, 4, 64, 2)  # d_head = 48
+    assert code == 0
+    good = ctypes.c_void_p(0x10000)
+    assert tp.tp_attention_heads(h, good, 1, 4, 1, None, None, 0, 0, good, None, 0, None) == 9
+    tp.tp_plan_destroy(h)

@@ -1,0 +1,192 @@
+"""GPU parity of each C-ABI call against the float64 oracle, on identical
+seeded inputs.  bf16 outputs are compared with the oracle rounded to bf16
+(the output's storage type); fp32 outputs with the exact oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.tp_oracle as o
+from helpers import (assert_close_bf16, assert_close_fp32, col_shards, np64, qkv_shards, unshard_cols,
+                     unshard_qkv)
+from tensor_transformer_layer_03_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+# (d_model, n_heads, d_ffn, tp, M): ragged M, several tiles, degrees 1..8
+SHAPES = [
+    (512, 8, 1536, 4, 200),
+    (512, 8, 1536, 1, 130),
+    (1024, 8, 2816, 8, 77),
+    (256, 4, 1024, 2, 1),
+    (4096, 32, 11008, 4, 256),
+]
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def _plan(tp_mod, d, H, f, deg, act="swiglu", dtype="bf16"):
+    return tp_mod.Plan(d, H, f, deg, act=act, dtype=dtype)
+
+
+def _packed(tp_mod, plan, shape, dtype, seed):
+    w = I.make_weights(shape, dtype, _gen(seed))
+    pw, _ = plan.sizes(1, 1)
+    packed = torch.empty(pw, dtype=torch.uint8, device=DEV)
+    plan.shard_weights({k: v.to(DEV) for k, v in w.items()}, packed)
+    return w, packed
+
+
+def _check(got, ref, dtype, what):
+    if dtype == "bf16":
+        return assert_close_bf16(got, ref, what)
+    return assert_close_fp32(got, ref, what)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
+def test_column_qkv(tp, d, H, f, deg, M, dtype):
+    plan = _plan(tp, d, H, f, deg, dtype=dtype)
+    shape = I.BlockShape(d, H, f, "swiglu")
+    w, packed = _packed(tp, plan, shape, dtype, 1)
+    x = I.make_matrix(M, d, dtype, _gen(2))
+    out = torch.empty(deg, M, 3 * d // deg, dtype=I.torch_dtype(dtype), device=DEV)
+    plan.column_linear(tp.TP_QKV, x.to(DEV), M, packed, out)
+    plan.sync_status()
+    ref = qkv_shards(o.linear(x, w["Wq"]), o.linear(x, w["Wk"]), o.linear(x, w["Wv"]), deg, H)
+    if dtype == "bf16":
+        ref = o.round_bf16(ref)
+    _check(out, ref, dtype, "QKV")
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
+def test_column_ffn_up(tp, d, H, f, deg, M, dtype, act):
+    plan = _plan(tp, d, H, f, deg, act=act, dtype=dtype)
+    shape = I.BlockShape(d, H, f, act)
+    w, packed = _packed(tp, plan, shape, dtype, 3)
+    h = I.make_matrix(M, d, dtype, _gen(4))
+    out = torch.empty(deg, M, f // deg, dtype=I.torch_dtype(dtype), device=DEV)
+    plan.column_linear(tp.TP_FFN_UP, h.to(DEV), M, packed, out)
+    plan.sync_status()
+    if act == "swiglu":
+        u = o.silu(o.linear(h, w["Wg"])) * o.linear(h, w["Wu"])
+    else:
+        u = o.gelu_erf(o.linear(h, w["W1"]))
+    ref = col_shards(u, deg)
+    if dtype == "bf16":
+        ref = o.round_bf16(ref)
+    _check(out, ref, dtype, f"FFN-up {act}")
+
+
+@pytest.mark.parametrize("which", ["attn_out", "ffn_down"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
+def test_row_reduce(tp, d, H, f, deg, M, dtype, which):
+    plan = _plan(tp, d, H, f, deg, dtype=dtype)
+    shape = I.BlockShape(d, H, f, "swiglu")
+    w, packed = _packed(tp, plan, shape, dtype, 5)
+    g = _gen(6)
+    ks = d // deg if which == "attn_out" else f // deg
+    inp = torch.stack([I.make_matrix(M, ks, dtype, g) for _ in range(deg)])
+    if which == "attn_out":
+        res = I.make_matrix(M, d, dtype, g)
+        W = w["Wo"]
+        code = tp.TP_ATTN_OUT
+    else:
+        res = I.make_matrix(M, d, "fp32", g)
+        W = w["Wd"]
+        code = tp.TP_FFN_DOWN
+    out = torch.empty(M, d, dtype=torch.float32, device=DEV)
+    out_act = torch.empty(M, d, dtype=I.torch_dtype(dtype), device=DEV)
+    plan.row_linear_reduce(code, inp.to(DEV), M, packed, res.to(DEV), out, out_act)
+    plan.sync_status()
+    a_full = unshard_cols(inp)
+    ref = np64(res) + o.all_reduce_sum(o.row_parallel_partials(a_full, W, deg))
+    # fp32 output: accumulation-order noise only
+    nw = float(np.max(np.abs(np64(out) - ref)) / np.max(np.abs(ref)))
+    assert nw <= 1e-5, nw
+    _check(out_act, o.round_bf16(ref) if dtype == "bf16" else ref, dtype, "row act copy")
+    # without residual and without the act copy
+    plan.row_linear_reduce(code, inp.to(DEV), M, packed, None, out, None)
+    plan.sync_status()
+    ref0 = ref - np64(res)
+    assert float(np.max(np.abs(np64(out) - ref0)) / np.max(np.abs(ref0))) <= 1e-5
+
+
+ATTN_CASES = [
+    # (d, H, deg, B, T, causal, q_scale)
+    (512, 4, 2, 2, 200, True, 1.0),
+    (512, 4, 4, 1, 333, False, 1.0),
+    (1024, 8, 8, 2, 129, True, 3.0),
+    (256, 4, 1, 1, 1, True, 1.0),
+    (256, 8, 2, 3, 64, True, 2.0),   # d_head 32
+    (4096, 32, 4, 1, 512, True, 1.0),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d,H,deg,B,T,causal,qs", ATTN_CASES)
+def test_attention_prefill(tp, d, H, deg, B, T, causal, qs, dtype):
+    plan = _plan(tp, d, H, 8 * deg, deg, dtype=dtype)
+    M = B * T
+    g = _gen(7)
+    qkv = torch.stack([I.make_matrix(M, 3 * d // deg, "fp32", g) for _ in range(deg)])
+    c = d // deg
+    qkv[:, :, :c] *= qs
+    qkv = qkv.to(I.torch_dtype(dtype))
+    out = torch.empty(deg, M, d // deg, dtype=I.torch_dtype(dtype), device=DEV)
+    plan.attention_heads(qkv.to(DEV), B, T, causal, None, None, 0, 0, out)
+    plan.sync_status()
+    q, k, v = unshard_qkv(qkv, deg)
+    ref = np.concatenate([o.multi_head_attention(q[b * T:(b + 1) * T], k[b * T:(b + 1) * T], v[b * T:(b + 1) * T],
+                                                 H, causal) for b in range(B)], axis=0)
+    ref = col_shards(ref, deg)
+    if dtype == "bf16":
+        ref = o.round_bf16(ref)
+    _check(out, ref, dtype, "attention")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d,H,deg,B,T,pos,cap", [
+    (512, 4, 2, 2, 1, 100, 128),     # single-token decode (split-KV)
+    (4096, 32, 2, 1, 1, 1024, 1025),  # the 7B decode shape
+    (512, 4, 4, 3, 1, 0, 8),         # first token
+    (512, 8, 2, 1, 1, 9000, 9001),   # more keys than 64 chunks of 128
+    (512, 4, 2, 2, 37, 50, 100),     # a chunk of tokens after a prefix
+])
+def test_attention_with_cache(tp, d, H, deg, B, T, pos, cap, dtype):
+    plan = _plan(tp, d, H, 8 * deg, deg, dtype=dtype)
+    dh = d // H
+    M = B * T
+    g = _gen(8)
+    qkv = torch.stack([I.make_matrix(M, 3 * d // deg, dtype, g) for _ in range(deg)])
+    kc = torch.randn(B, H, cap, dh, generator=g).to(I.torch_dtype(dtype))
+    vc = torch.randn(B, H, cap, dh, generator=g).to(I.torch_dtype(dtype))
+    kc_d, vc_d = kc.to(DEV), vc.to(DEV)
+    out = torch.empty(deg, M, d // deg, dtype=I.torch_dtype(dtype), device=DEV)
+    nscr = plan.attention_scratch_bytes(B, T, cap)
+    scratch = torch.empty(max(nscr, 16), dtype=torch.uint8, device=DEV)
+    plan.attention_heads(qkv.to(DEV), B, T, True, kc_d, vc_d, cap, pos, out, scratch)
+    plan.sync_status()
+    q, k, v = unshard_qkv(qkv, deg)
+    refs = []
+    for b in range(B):
+        kk = np.concatenate([np64(kc[b, :, :pos]).transpose(1, 0, 2).reshape(pos, d), k[b * T:(b + 1) * T]])
+        vv = np.concatenate([np64(vc[b, :, :pos]).transpose(1, 0, 2).reshape(pos, d), v[b * T:(b + 1) * T]])
+        refs.append(o.multi_head_attention(q[b * T:(b + 1) * T], kk, vv, H, True, q_pos0=pos))
+    ref = col_shards(np.concatenate(refs, axis=0), deg)
+    if dtype == "bf16":
+        ref = o.round_bf16(ref)
+    _check(out, ref, dtype, "cached attention")
+    # the new tokens' K/V landed in the cache at pos.., the rest is untouched
+    kn = np64(kc_d.cpu())
+    for b in range(B):
+        new = k[b * T:(b + 1) * T].reshape(T, H, dh).transpose(1, 0, 2)
+        assert np.array_equal(kn[b, :, pos:pos + T], new)
+        assert np.array_equal(kn[b, :, :pos], np64(kc[b, :, :pos]))
+        assert np.array_equal(kn[b, :, pos + T:], np64(kc[b, :, pos + T:]))
