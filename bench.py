@@ -1,0 +1,352 @@
+"""Benchmark of the tensor-parallel block on B300.
+
+A step is one pass of the whole block (column QKV -> per-shard attention ->
+row-parallel O + reduce -> column FFN-up + SwiGLU -> row-parallel FFN-down +
+reduce) over one batch of the LLaMA-2-7B-shaped prefill workload
+(d_model 4096, 32 heads, d_ffn 11008, tp 4 logical shards, batch 1 x 2048
+tokens, causal, bf16), inputs resident in HBM.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs one independent replica per GPU (launched by torchrun); the
+block does not shard across GPUs here (its shards are logical partitions of
+one GPU), so ranks exchange nothing but the timing.  ``--impl reference``
+times the float64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and TFLOP/s (prefill), HBM GB/s (decode) per TP block on 1 B300 vs roofline"
+L2_FLUSH_BYTES = 256 << 20  # > 126 MB L2
+
+
+def block_flops(wl):
+    s = wl.shape
+    d, f, B, T = s.d_model, s.d_ffn, wl.batch, wl.seq
+    lin = 2.0 * B * T * (4 * d * d + 3 * d * f)
+    # QK^T and PV over the visible keys (causal: T(T+1)/2 per head-row sum)
+    keys = T * (T + 1) / 2 if wl.causal else T * T
+    attn = 4.0 * d * B * keys
+    return lin, attn
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(ngpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("TP_BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(value, pg, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the float64 CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def time_oracle(wl, sample_tokens, steps, warmup=0):
+    """Seconds per oracle call on the first `sample_tokens` tokens of the
+    workload (causal: those tokens form a self-contained prefix)."""
+    import oracle
+    from tensor_transformer_layer_03_b300 import inputs as I
+    inp = I.make_inputs(wl)
+    w = {k: v for k, v in inp.items() if k.startswith("W")}
+    w = {k: oracle.to64(v) for k, v in w.items()}
+    x = oracle.to64(inp["X"][:1, :sample_tokens])
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        oracle.block_forward(x, w, wl.shape.n_heads, wl.shape.act, wl.causal)
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    return times
+
+
+def run_reference(args):
+    world, rank, local, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None
+    if rank != 0:
+        return 0
+    from tensor_transformer_layer_03_b300 import inputs as I
+    wl = I.WORKLOADS["llama7b_prefill"]
+    sample = 256
+    times = time_oracle(wl, sample, args.steps, args.warmup)
+    total = sum(times)
+    value = sample * len(times) / total
+    cores = oracle_cores()
+    sample_desc = (f"first {sample} of the {wl.seq} tokens of the 7B-shaped prefill block per step "
+                   f"(causal prefix, float64 numpy oracle)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama7b_prefill", "d_model": 4096, "n_heads": 32, "d_ffn": 11008,
+                   "tp_degree": wl.tp, "batch": wl.batch, "seq": wl.seq, "causal": True},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    from tensor_transformer_layer_03_b300 import inputs as I
+    from tensor_transformer_layer_03_b300 import tp as tpb
+    from tensor_transformer_layer_03_b300.runtime import TPBlock
+
+    world, rank, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = I.WORKLOADS[args.workload]
+    inp = I.make_inputs(wl, seed=0)
+    w = {k: v for k, v in inp.items() if k.startswith("W")}
+    blk = TPBlock(wl.shape, wl.tp, wl.dtype, w, device=dev, max_batch=wl.batch, max_seq=wl.seq)
+    plan = blk.plan
+    B, T, d = wl.batch, wl.seq, wl.shape.d_model
+    M = B * T
+    x = inp["X"].to(dev)
+    del inp, w
+    stream = torch.cuda.Stream(device=dev)
+    h = plan.h_l * plan.d_head
+    qkv = torch.empty(wl.tp, M, 3 * h, dtype=torch.bfloat16, device=dev)
+    att = torch.empty(wl.tp, M, h, dtype=torch.bfloat16, device=dev)
+    hf = torch.empty(M, d, dtype=torch.float32, device=dev)
+    ha = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    u = torch.empty(wl.tp, M, plan.f_l, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(M, d, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stages = ["column_qkv", "attention", "row_o_reduce", "column_ffn_up_swiglu", "row_ffn_down_reduce"]
+
+    def step(ev):
+        ev[0].record(stream)
+        plan.column_linear(tpb.TP_QKV, x, M, blk.packed, qkv, stream)
+        ev[1].record(stream)
+        plan.attention_heads(qkv, B, T, wl.causal, None, None, 0, 0, att, None, stream)
+        ev[2].record(stream)
+        plan.row_linear_reduce(tpb.TP_ATTN_OUT, att, M, blk.packed, x, hf, ha, stream)
+        ev[3].record(stream)
+        plan.column_linear(tpb.TP_FFN_UP, ha, M, blk.packed, u, stream)
+        ev[4].record(stream)
+        plan.row_linear_reduce(tpb.TP_FFN_DOWN, u, M, blk.packed, hf, y, None, stream)
+        ev[5].record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps + args.warmup)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            step(evs[i])
+        stream.synchronize()
+        plan.sync_status(stream)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as clk:
+            t_wall0 = time.perf_counter()
+            for i in range(args.warmup, args.warmup + args.steps):
+                flush.fill_(i & 0xFF)  # evicts the previous step's lines from L2 (outside the step's events)
+                step(evs[i])
+            stream.synchronize()
+            t_wall = time.perf_counter() - t_wall0
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+    plan.sync_status(stream)
+    per_stage = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.warmup, args.warmup + args.steps)]
+                 for j in range(5)]
+    step_ms = [sum(per_stage[j][k] for j in range(5)) for k in range(args.steps)]
+    dev_ms_total = sum(step_ms)
+    dev_ms_total = max_over_ranks(dev_ms_total, pg, dev)
+    ms_per_step = dev_ms_total / args.steps
+    tokens = M * args.steps * world
+    value = tokens / (dev_ms_total / 1000.0)
+    lin, attn = block_flops(wl)
+    tflops = (lin + attn) / (ms_per_step / 1000.0) / 1e12
+
+    # dominant kernel: the stage with the largest mean time
+    stage_mean = [statistics.mean(s) for s in per_stage]
+    dom = max(range(5), key=lambda j: stage_mean[j])
+    s = wl.shape
+    stage_flops = [2.0 * M * d * 3 * d, attn, 2.0 * M * d * d, 2.0 * M * d * 2 * s.d_ffn, 2.0 * M * s.d_ffn * d]
+    pk = peaks()
+    achieved = stage_flops[dom] / (stage_mean[dom] / 1000.0) / 1e12
+    roofline = {"bound": "tensor", "kernel": stages[dom], "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                "peak_source": f"{pk['source']} bf16 dense burst (cuBLAS)"}
+
+    # end to end through the public call: pinned host x in, Y out
+    if True:
+        xh = x.cpu().pin_memory()
+        yh = torch.empty(M, d, dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(x)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                xd.copy_(xh, non_blocking=True)
+                blk.forward(xd, wl.causal, out=y.view(B, T, d), stream=stream)
+                yh.copy_(y, non_blocking=True)
+            stream.synchronize()
+            tot = 0.0
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                e0[i].record(stream)
+                xd.copy_(xh, non_blocking=True)
+                blk.forward(xd, wl.causal, out=y.view(B, T, d), stream=stream)
+                yh.copy_(y, non_blocking=True)
+                e0[i + 1].record(stream)
+                stream.synchronize()
+                tot += e0[i].elapsed_time(e0[i + 1])
+        plan.sync_status(stream)
+        tot = max_over_ranks(tot, pg, dev)
+        e2e = {"value": M * args.steps * world / (tot / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": y.numel() * 4,
+               "ms_per_step": tot / args.steps}
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
+        sample = 256
+        times = time_oracle(wl, sample, 1)
+        cpu = {"value": sample / times[0], "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
+               "sample": f"first {sample} of the {T} tokens of the same block (causal prefix), one float64 call"}
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "d_model": d, "n_heads": s.n_heads, "d_ffn": s.d_ffn,
+                       "tp_degree": wl.tp, "batch": B, "seq": T, "causal": wl.causal, "act": s.act,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "flushed between steps (256 MB write)"},
+            "tflops": tflops,
+            "tflops_frac_of_peak": tflops / pk["bf16_tflops"],
+            "stage_ms": {n: m for n, m in zip(stages, stage_mean)},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 5 * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama7b_prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -190,7 +190,7 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
     const int n_out = qkv ? N : p->fl;                     // output columns per shard
     const void* W = ptr_at(packed, qkv ? p->off_qkv : p->off_up);
     const int epi = qkv ? tpk::EPI_STORE : (p->act == TP_ACT_SWIGLU ? tpk::EPI_SWIGLU : tpk::EPI_GELU);
-    if (p->dtype == TP_BF16 && tpk::tc_gemm_supported(M, N, p->d)) {
+    if (p->dtype == TP_BF16 && tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32)) {
         tpk::TcGemm g{};
         g.epi = epi;
         g.A = x;
