@@ -107,15 +107,18 @@ def test_row_reduce(tp, d, H, f, deg, M, dtype, which):
     plan.sync_status()
     a_full = unshard_cols(inp)
     ref = np64(res) + o.all_reduce_sum(o.row_parallel_partials(a_full, W, deg))
-    # fp32 output: accumulation-order noise only
+    # fp32 output: accumulation-order noise only.  fp32 plans: <= 1e-5; bf16
+    # plans accumulate in the tensor cores' fp32 over K = tp * k_s terms:
+    # bound 1e-4 (sqrt(11008) * 2^-24 * a few, with room)
+    fp32_bound = 1e-5 if dtype == "fp32" else 1e-4
     nw = float(np.max(np.abs(np64(out) - ref)) / np.max(np.abs(ref)))
-    assert nw <= 1e-5, nw
+    assert nw <= fp32_bound, nw
     _check(out_act, o.round_bf16(ref) if dtype == "bf16" else ref, dtype, "row act copy")
     # without residual and without the act copy
     plan.row_linear_reduce(code, inp.to(DEV), M, packed, None, out, None)
     plan.sync_status()
     ref0 = ref - np64(res)
-    assert float(np.max(np.abs(np64(out) - ref0)) / np.max(np.abs(ref0))) <= 1e-5
+    assert float(np.max(np.abs(np64(out) - ref0)) / np.max(np.abs(ref0))) <= fp32_bound
 
 
 ATTN_CASES = [
