@@ -16,6 +16,7 @@ times the float64 CPU oracle on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -51,27 +52,38 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms; only the
+    samples stamped inside the timed window [mark_start, mark_end] count."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.out = ""
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        time.sleep(1.0)  # let nvidia-smi come up before the timed region
         return self
 
-    def __exit__(self, *exc):
-        self.out = ""
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
+
+    def stop(self):
         if self.proc is not None:
+            time.sleep(0.3)
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)
@@ -80,24 +92,30 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons, power = [], [], set(), []
         for line in (self.out or "").splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            if self.t0 is None or self.t1 is None or not (self.t0 <= ts <= self.t1):
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
+                power.append(float(f[4]))
+            except ValueError:
+                continue
+            for n, v in zip(self.NAMES, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_median": statistics.median(power)}
 
 
 def dist_setup(ngpus):
@@ -155,24 +173,29 @@ def time_oracle(wl, sample_tokens, steps, warmup=0):
 
 
 def run_reference(args):
-    world, rank, local, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None
+    rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
-        return 0
+        return 0  # the oracle runs once, on rank 0's host cores
     from tensor_transformer_layer_03_b300 import inputs as I
-    wl = I.WORKLOADS["llama7b_prefill"]
-    sample = 256
+    wl = I.WORKLOADS[args.workload]
+    # size each step's sample so that warmup + steps take about 90 s
+    probe = time_oracle(wl, 128, 1)[0]
+    per_token = probe / 128
+    sample = int(90.0 / (args.steps + args.warmup) / per_token) // 64 * 64
+    sample = max(64, min(wl.seq, sample))
     times = time_oracle(wl, sample, args.steps, args.warmup)
     total = sum(times)
     value = sample * len(times) / total
     cores = oracle_cores()
-    sample_desc = (f"first {sample} of the {wl.seq} tokens of the 7B-shaped prefill block per step "
-                   f"(causal prefix, float64 numpy oracle)")
+    sample_desc = (f"first {sample} of the {wl.seq} tokens of the same block per step "
+                   f"(causal prefix), float64 numpy oracle")
+    s = wl.shape
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "llama7b_prefill", "d_model": 4096, "n_heads": 32, "d_ffn": 11008,
-                   "tp_degree": wl.tp, "batch": wl.batch, "seq": wl.seq, "causal": True},
+        "config": {"workload": args.workload, "d_model": s.d_model, "n_heads": s.n_heads, "d_ffn": s.d_ffn,
+                   "tp_degree": wl.tp, "batch": wl.batch, "seq": wl.seq, "causal": wl.causal, "act": s.act},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -228,6 +251,7 @@ def run_ours(args):
         ev[5].record(stream)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps + args.warmup)]
+    clk = ClockSampler(local).start()
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             flush.fill_(i & 0xFF)
@@ -237,13 +261,15 @@ def run_ours(args):
         if pg is not None:
             pg.barrier()
         torch.cuda.synchronize(dev)
-        with ClockSampler(local) as clk:
-            t_wall0 = time.perf_counter()
-            for i in range(args.warmup, args.warmup + args.steps):
-                flush.fill_(i & 0xFF)  # evicts the previous step's lines from L2 (outside the step's events)
-                step(evs[i])
-            stream.synchronize()
-            t_wall = time.perf_counter() - t_wall0
+        clk.mark_start()
+        t_wall0 = time.perf_counter()
+        for i in range(args.warmup, args.warmup + args.steps):
+            flush.fill_(i & 0xFF)  # evicts the previous step's lines from L2 (outside the step's events)
+            step(evs[i])
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        clk.mark_end()
+        clk.stop()
         torch.cuda.synchronize(dev)
         if pg is not None:
             pg.barrier()
@@ -299,11 +325,10 @@ def run_ours(args):
                "ms_per_step": tot / args.steps}
 
     cpu = None
-    if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
-        sample = 256
-        times = time_oracle(wl, sample, 1)
-        cpu = {"value": sample / times[0], "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
-               "sample": f"first {sample} of the {T} tokens of the same block (causal prefix), one float64 call"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times = time_oracle(wl, T, 2)
+        cpu = {"value": M * len(times) / sum(times), "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
+               "sample": f"the whole workload ({B} x {T} tokens), float64 numpy oracle, 2 calls"}
 
     clocks = clk.summary()
     if rank == 0:
@@ -335,7 +360,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama7b_prefill")
