@@ -190,6 +190,32 @@ tp_status tp_attention_heads(tp_plan_t plan, const void* qkv_shards, int batch, 
                              size_t scratch_bytes, void* stream);
 
 /*
+ * Single-token decode attention that allocates nothing and takes no scratch
+ * buffer.  (The pages have no counterpart: this serves callers that cannot
+ * allocate device memory on their decode path -- code running inside a
+ * memory pool it does not own, a host framework that forbids cudaMalloc
+ * there, or a process whose allocator is exhausted.)
+ * Same result as tp_attention_heads(plan, qkv_shards, batch, 1, causal=1,
+ * k_cache, v_cache, cache_cap, cache_pos, out_shards, scratch, ...): the new
+ * token's K/V are written at cache_pos and each head attends over positions
+ * 0..cache_pos.  The split-KV partials go to a fixed 8 MiB device array
+ * inside the library (held by every GPU that loads it until process exit)
+ * instead of `scratch`; batch * n_heads * 64 * (d_head + 2) * 4 bytes must
+ * fit in it, else TP_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued.
+ *  - The first call on each device looks up that array's device address
+ *    (cudaGetSymbolAddress, with the device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array, so calls that can overlap
+ *    on the GPU (different streams, no ordering between them) race and give
+ *    wrong results; order them on one stream or with events.
+ *  - The array keeps the last call's partials; every call rewrites what it
+ *    reads, so no clearing is needed.
+ */
+tp_status tp_attention_decode_noalloc(tp_plan_t plan, const void* qkv_shards, int batch,
+                                      void* k_cache, void* v_cache, int cache_cap, int cache_pos,
+                                      void* out_shards, void* stream);
+
+/*
  * The whole block: column QKV, attention, row O + reduce (+x), column
  * FFN-up + activation, row FFN-down + reduce (+H).
  *   x         device act [batch*seq][d_model]

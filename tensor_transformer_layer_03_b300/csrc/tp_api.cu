@@ -9,19 +9,12 @@
 #include <new>
 
 #include "kernels.h"
+#include "plan.h"
 #include "tp.h"
 
 // First device-side error recorded by a bounded wait (0 = none).  Kernels
 // receive its address; tp_sync_status reads and clears it.
 __device__ int g_tp_device_error;
-
-struct tp_plan_s {
-    int d, H, dh, f, tp, hl, fl, granule, up_rows;
-    tp_act act;
-    tp_dtype dtype;
-    int esize;
-    size_t off_qkv, off_o, off_up, off_down, packed_bytes;
-};
 
 namespace {
 
@@ -29,13 +22,9 @@ thread_local char g_last_cuda_error[256] = "";
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+bool misaligned(const void* p) { return tpk::misaligned16(p); }
 
-tp_status cuda_status(cudaError_t e) {
-    if (e == cudaSuccess) return TP_OK;
-    strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
-    return TP_ERR_CUDA;
-}
+tp_status cuda_status(cudaError_t e) { return tpk::status_from_cuda(e); }
 
 int* device_error_word() {
     int dev = 0;
@@ -77,6 +66,12 @@ const char* ptr_at(const void* base, size_t off) { return static_cast<const char
 char* ptr_at(void* base, size_t off) { return static_cast<char*>(base) + off; }
 
 }  // namespace
+
+tp_status tpk::status_from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return TP_OK;
+    strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
+    return TP_ERR_CUDA;
+}
 
 extern "C" {
 

@@ -49,6 +49,7 @@ EXPORTS = {
     "tp_row_linear_reduce": (_i, [_p, _i, _p, _i, _p, _p, _p, _p, _p]),
     "tp_attention_heads": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p]),
     "tp_block_forward": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p, _p]),
+    "tp_attention_decode_noalloc": (_i, [_p, _p, _i, _p, _p, _i, _i, _p, _p]),
     "tp_sync_status": (_i, [_p]),
 }
 for _name, (_res, _args) in EXPORTS.items():
@@ -152,6 +153,10 @@ class Plan:
         check(tp_block_forward(self.handle, _ptr(x), batch, seq, int(causal), _ptr(k_cache), _ptr(v_cache),
                                cache_cap, cache_pos, _ptr(packed), _ptr(workspace), nbytes, _ptr(out_f32),
                                _stream(stream)), "tp_block_forward")
+
+    def attention_decode_noalloc(self, qkv, batch, k_cache, v_cache, cache_cap, cache_pos, out, stream=None):
+        check(tp_attention_decode_noalloc(self.handle, _ptr(qkv), batch, _ptr(k_cache), _ptr(v_cache), cache_cap,
+                                          cache_pos, _ptr(out), _stream(stream)), "tp_attention_decode_noalloc")
 
     def sync_status(self, stream=None):
         check(tp_sync_status(_stream(stream)), "tp_sync_status")
