@@ -68,7 +68,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -207,6 +207,62 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
+def bench_decode(args, dev, flush):
+    """One-token decode step of the 7B-shaped block (tp 2, 1024 cached
+    positions + the new one), captured in a CUDA graph; HBM GB/s against the
+    algorithmic bytes (every packed weight once + the K/V cache read)."""
+    import torch
+
+    from tensor_transformer_layer_03_b300 import inputs as I
+    from tensor_transformer_layer_03_b300.runtime import TPBlock
+    wl = I.WORKLOADS["llama7b_decode"]
+    inp = I.make_inputs(wl, seed=0)
+    w = {k: v for k, v in inp.items() if k.startswith("W")}
+    s = wl.shape
+    B, P = wl.batch, wl.cache_len
+    cap = P + 1
+    blk = TPBlock(s, wl.tp, wl.dtype, w, device=dev, max_batch=B, max_seq=1)
+    kc = torch.zeros(B, s.n_heads, cap, s.d_head, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    kc[:, :, :P] = inp["Kcache"].to(dev)
+    vc[:, :, :P] = inp["Vcache"].to(dev)
+    x = inp["X"].to(dev)
+    y = torch.empty(B, 1, s.d_model, dtype=torch.float32, device=dev)
+    del inp, w
+    st = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            blk.forward(x, True, out=y, k_cache=kc, v_cache=vc, cache_pos=P, stream=st)
+        st.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            blk.forward(x, True, out=y, k_cache=kc, v_cache=vc, cache_pos=P, stream=st)
+        st.synchronize()
+        n = max(50, args.steps // 2)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(3):
+            graph.replay()
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(st)
+            graph.replay()
+            evs[i][1].record(st)
+        st.synchronize()
+    blk.plan.sync_status(st)
+    us = [a.elapsed_time(b) * 1000.0 for a, b in evs]
+    d, f = s.d_model, s.d_ffn
+    weight_bytes = 2 * (4 * d * d + 3 * d * f)
+    kv_bytes = 2 * B * s.n_heads * (P + 1) * s.d_head * 2
+    algo = weight_bytes + kv_bytes
+    med = statistics.median(us)
+    gbs = algo / (med * 1e-6) / 1e9
+    pk = peaks()
+    return {"workload": "llama7b_decode", "tp_degree": wl.tp, "batch": B, "cache_positions": P + 1,
+            "us_per_step_median": med, "us_per_step_p10": sorted(us)[len(us) // 10],
+            "algorithmic_bytes": algo, "gb_s": gbs, "hbm_peak_gb_s": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
+            "graph": True, "launches_per_step": 7, "l2": "flushed between steps"}
+
+
 def run_ours(args):
     import torch
 
@@ -324,6 +380,8 @@ def run_ours(args):
                "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": y.numel() * 4,
                "ms_per_step": tot / args.steps}
 
+    decode = bench_decode(args, dev, flush) if not args.no_decode else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = time_oracle(wl, T, 2)
@@ -344,6 +402,7 @@ def run_ours(args):
             "tflops_frac_of_peak": tflops / pk["bf16_tflops"],
             "stage_ms": {n: m for n, m in zip(stages, stage_mean)},
             "roofline": roofline,
+            "decode": decode,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 5 * args.steps,
@@ -360,11 +419,12 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama7b_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

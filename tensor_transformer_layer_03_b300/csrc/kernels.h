@@ -78,6 +78,13 @@ struct TcGemm {
 bool tc_gemm_supported(int M, int N, int K);
 cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st);
 
+// ---- small-M weight streaming (gemv.cu): same arguments as the GEMM ---------
+typedef TcGemm GemvArgs;
+constexpr int GEMV_MAX_M = 8;
+bool gemv_supported(const GemvArgs& g);
+size_t gemv_smem_bytes(const GemvArgs& g);
+cudaError_t gemv(const GemvArgs& g, cudaStream_t st);
+
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
 bool tc_attention_supported(const AttnArgs& a);
 cudaError_t tc_attention(const AttnArgs& a, cudaStream_t st);

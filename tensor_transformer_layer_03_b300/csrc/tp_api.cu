@@ -185,7 +185,7 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
     const int n_out = qkv ? N : p->fl;                     // output columns per shard
     const void* W = ptr_at(packed, qkv ? p->off_qkv : p->off_up);
     const int epi = qkv ? tpk::EPI_STORE : (p->act == TP_ACT_SWIGLU ? tpk::EPI_SWIGLU : tpk::EPI_GELU);
-    if (p->dtype == TP_BF16 && tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32)) {
+    if (p->dtype == TP_BF16) {
         tpk::TcGemm g{};
         g.epi = epi;
         g.A = x;
@@ -202,7 +202,9 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
         g.out_shard = (long long)M * n_out;
         g.ldo = n_out;
         g.granule = p->granule;
-        return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
+        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, st));
+        if (tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32))
+            return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
     }
     tpk::SimtGemm g{};
     g.epi = epi;
@@ -237,7 +239,7 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
     const int ks = attn ? p->hl * p->dh : p->fl;
     const void* W = ptr_at(packed, attn ? p->off_o : p->off_down);
     const int res_f32 = attn ? (p->dtype == TP_FP32) : 1;
-    if (p->dtype == TP_BF16 && tpk::tc_gemm_supported(M, p->d, ks)) {
+    if (p->dtype == TP_BF16) {
         tpk::TcGemm g{};
         g.epi = tpk::EPI_ROW_REDUCE;
         g.A = in_shards;
@@ -255,7 +257,8 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
         g.out2 = out_act;
         g.residual = residual;
         g.residual_f32 = res_f32;
-        return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
+        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, st));
+        if (tpk::tc_gemm_supported(M, p->d, ks)) return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
     }
     tpk::SimtGemm g{};
     g.epi = tpk::EPI_ROW_REDUCE;

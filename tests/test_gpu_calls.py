@@ -21,6 +21,10 @@ SHAPES = [
     (1024, 8, 2816, 8, 77),
     (256, 4, 1024, 2, 1),
     (4096, 32, 11008, 4, 256),
+    # small M: the weight-streaming (decode) kernels
+    (4096, 32, 11008, 2, 1),
+    (4096, 32, 11008, 8, 8),
+    (512, 8, 1536, 4, 5),
 ]
 
 
