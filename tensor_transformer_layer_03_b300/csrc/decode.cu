@@ -111,16 +111,148 @@ __global__ void __launch_bounds__(DH) decode_combine_k(AttnArgs a, const float* 
     out[threadIdx.x] = from_f<T>(o / l);
 }
 
+// bf16 variant of pass 1 with 16-byte loads: DH/8 lanes share a key row
+// (each lane one 16-byte slice), so a warp scores 32/(DH/8) keys per step
+// with fully coalesced loads; the chunk is walked in sub-chunks of SUB keys
+// with the online max/sum; in the P.V pass each lane owns DH/32 dimensions
+// and the four warps take interleaved keys.
+constexpr int SUB = 256;
+
+// DPL consecutive bf16 (DPL = 1, 2 or 4; 2*DPL-byte aligned) as floats
+template <int DPL>
+__device__ __forceinline__ void load_dims(const bf16* p, float (&f)[DPL]) {
+    if constexpr (DPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+        f[0] = a.x;
+        f[1] = a.y;
+        f[2] = b.x;
+        f[3] = b.y;
+    } else if constexpr (DPL == 2) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+        f[0] = a.x;
+        f[1] = a.y;
+    } else {
+        f[0] = __bfloat162float(p[0]);
+    }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(DEC_THREADS) decode_split_bf16_k(AttnArgs a, float* __restrict__ part, int chunk) {
+    constexpr int LPK = DH / 8;    // lanes per key row
+    constexpr int KPW = 32 / LPK;  // keys per warp step
+    constexpr int DPL = DH / 32;   // output dims per lane
+    constexpr int NW = DEC_THREADS / 32;
+    __shared__ float sc[SUB];
+    __shared__ float red[NW];
+    __shared__ float ored[NW][DH];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int s = h / a.hl, jl = h % a.hl;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int sub_l = lane % LPK, kq = lane / LPK;
+    const bf16* q = (const bf16*)a.qkv + ((long long)s * a.B + b) * (3 * a.hl * DH) + jl * DH;
+    float qv[8];
+    {
+        const uint4 v = *reinterpret_cast<const uint4*>(q + sub_l * 8);
+        const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(hq[i]);
+            qv[2 * i] = f.x * a.scale;
+            qv[2 * i + 1] = f.y * a.scale;
+        }
+    }
+    const int L = a.pos + 1;
+    const int k0 = c * chunk, k1 = min(L, k0 + chunk);
+    const bf16* kbase = (const bf16*)a.kc + ((long long)b * a.H + h) * a.cap * DH;
+    const bf16* vbase = (const bf16*)a.vc + ((long long)b * a.H + h) * a.cap * DH;
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+
+    for (int sub = k0; sub < k1; sub += SUB) {
+        const int n = min(SUB, k1 - sub);
+        for (int j0 = warp * KPW; j0 < n; j0 += NW * KPW) {
+            const int j = j0 + kq;
+            float d = 0.f;
+            if (j < n) {
+                const uint4 v = *reinterpret_cast<const uint4*>(kbase + (long long)(sub + j) * DH + sub_l * 8);
+                const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(hk[i]);
+                    d = fmaf(qv[2 * i], f.x, d);
+                    d = fmaf(qv[2 * i + 1], f.y, d);
+                }
+            }
+#pragma unroll
+            for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            if (sub_l == 0 && j < n) sc[j] = d;
+        }
+        __syncthreads();
+        float mt = -INFINITY;
+        for (int j = threadIdx.x; j < n; j += DEC_THREADS) mt = fmaxf(mt, sc[j]);
+        mt = block_reduce(mt, red, true);
+        const float mnew = fmaxf(m_run, mt);
+        float lt = 0.f;
+        for (int j = threadIdx.x; j < n; j += DEC_THREADS) {
+            const float p = expf(sc[j] - mnew);
+            sc[j] = p;
+            lt += p;
+        }
+        lt = block_reduce(lt, red, false);  // its barriers also publish sc[]
+        const float corr = m_run == -INFINITY ? 0.f : expf(m_run - mnew);
+        l_run = l_run * corr + lt;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] *= corr;
+        for (int j = warp; j < n; j += NW) {
+            const float p = sc[j];
+            float v[DPL];
+            load_dims<DPL>(vbase + (long long)(sub + j) * DH + lane * DPL, v);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[e] = fmaf(p, v[e], o[e]);
+        }
+        m_run = mnew;
+        __syncthreads();  // sc[] is rewritten by the next sub-chunk
+    }
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) ored[warp][lane * DPL + e] = o[e];
+    __syncthreads();
+    float* dst = part + (((long long)b * a.H + h) * DECODE_MAX_SPLITS + c) * (DH + 2);
+    for (int i = threadIdx.x; i < DH; i += DEC_THREADS) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2) acc += ored[w2][i];
+        dst[2 + i] = acc;
+    }
+    if (threadIdx.x == 0) {
+        dst[0] = m_run;
+        dst[1] = l_run;
+    }
+}
+
 template <typename T, int DH>
 cudaError_t decode_launch(const AttnArgs& a, float* scratch, cudaStream_t st) {
     const int L = a.pos + 1;
-    int nsplit = (L + DEC_THREADS - 1) / DEC_THREADS;
-    int chunk = DEC_THREADS;
-    if (nsplit > DECODE_MAX_SPLITS) {
-        chunk = ((L + DECODE_MAX_SPLITS - 1) / DECODE_MAX_SPLITS + DEC_THREADS - 1) / DEC_THREADS * DEC_THREADS;
+    int nsplit, chunk;
+    if (a.is_bf16) {
+        // chunks of about 64 keys, at most DECODE_MAX_SPLITS of them
+        nsplit = (L + 63) / 64;
+        if (nsplit > DECODE_MAX_SPLITS) nsplit = DECODE_MAX_SPLITS;
+        chunk = (L + nsplit - 1) / nsplit;
         nsplit = (L + chunk - 1) / chunk;
+        decode_split_bf16_k<DH><<<dim3(nsplit, a.H, a.B), DEC_THREADS, 0, st>>>(a, scratch, chunk);
+    } else {
+        nsplit = (L + DEC_THREADS - 1) / DEC_THREADS;
+        chunk = DEC_THREADS;
+        if (nsplit > DECODE_MAX_SPLITS) {
+            chunk = ((L + DECODE_MAX_SPLITS - 1) / DECODE_MAX_SPLITS + DEC_THREADS - 1) / DEC_THREADS * DEC_THREADS;
+            nsplit = (L + chunk - 1) / chunk;
+        }
+        decode_split_k<T, DH><<<dim3(nsplit, a.H, a.B), DEC_THREADS, 0, st>>>(a, scratch, chunk, nsplit);
     }
-    decode_split_k<T, DH><<<dim3(nsplit, a.H, a.B), DEC_THREADS, 0, st>>>(a, scratch, chunk, nsplit);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_combine_k<T, DH><<<dim3(a.H, a.B), DH, 0, st>>>(a, scratch, nsplit);

@@ -3,13 +3,16 @@
 // With one to a few tokens per step every weight element is used M times, so
 // the linears are bound by reading the packed weights once from HBM.  Each
 // warp owns whole weight rows and streams them with 16-byte non-allocating
-// loads (four in flight per lane); the M input rows sit in shared memory.
+// loads, eight in flight per lane; the M input rows are read through the
+// read-only cache (every warp of the GPU reads the same few KB, so they stay
+// in L1/L2).  Kernels are specialised on the number of token rows so the
+// registers go to loads in flight, not to unused accumulators.
 //
 //  * column-parallel (undercodenews.com/?p=110319, "the Original": every
 //    shard multiplies the full input by its slice of the output features):
-//    all shards' rows form one list; SwiGLU rows come in gate/up blocks of 32
-//    (the packing's interleave), so a warp takes a gate row and its up row
-//    and writes silu(gate) * up.
+//    all shards' rows form one list; SwiGLU rows come in gate/up blocks (the
+//    packing's interleave), so a warp takes a gate row and its up row and
+//    writes silu(gate) * up.
 //  * row-parallel with the all-reduce fused in (same section): the warp that
 //    owns output feature n walks row n of every shard's weight block in
 //    shard order and sums the partial dot products in registers.
@@ -22,6 +25,7 @@ namespace {
 
 constexpr int GV_THREADS = 256;
 constexpr int GV_WARPS = GV_THREADS / 32;
+constexpr int GV_UNROLL = 8;  // 16-byte weight loads in flight per lane
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
     uint4 v;
@@ -31,14 +35,18 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+__device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
+    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&w);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
+    float s = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
+        const float2 fa = __bfloat1622float2(a[i]);
+        const float2 fb = __bfloat1622float2(b[i]);
+        s = fmaf(fa.x, fb.x, s);
+        s = fmaf(fa.y, fb.y, s);
     }
+    return s;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -47,151 +55,97 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// dot products of one weight row (K bf16, 16-byte aligned) with M input rows
-// held in shared memory as fp32 [M][K]; partial sums per lane.
-template <int MAXM>
-__device__ __forceinline__ void row_dots(const bf16* w, const float* xs, int K, int M, float (&acc)[MAXM]) {
+// Per-lane partial dot products of one weight row (K bf16) with MT input
+// rows x[m][0..K) (row stride ldx), accumulated into acc.
+template <int MT>
+__device__ __forceinline__ void row_dots(const bf16* __restrict__ w, const bf16* __restrict__ x, long long ldx,
+                                         int K, float (&acc)[MT]) {
     const int lane = threadIdx.x % 32;
     const int nch = K / 8;
     int c = lane;
-    for (; c + 96 < nch; c += 128) {
-        uint4 v[4];
+    for (; c + 32 * (GV_UNROLL - 1) < nch; c += 32 * GV_UNROLL) {
+        uint4 v[GV_UNROLL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = ld_stream(w + (c + 32 * u) * 8);
+        for (int u = 0; u < GV_UNROLL; ++u) v[u] = ld_stream(w + (c + 32 * u) * 8);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float f[8];
-            bf16x8_to_f32(v[u], f);
-            const int k = (c + 32 * u) * 8;
+        for (int u = 0; u < GV_UNROLL; ++u) {
 #pragma unroll
-            for (int m = 0; m < MAXM; ++m) {
-                if (m < M) {
-                    const float4 x0 = *reinterpret_cast<const float4*>(xs + m * K + k);
-                    const float4 x1 = *reinterpret_cast<const float4*>(xs + m * K + k + 4);
-                    acc[m] += f[0] * x0.x + f[1] * x0.y + f[2] * x0.z + f[3] * x0.w + f[4] * x1.x + f[5] * x1.y +
-                              f[6] * x1.z + f[7] * x1.w;
-                }
-            }
+            for (int m = 0; m < MT; ++m)
+                acc[m] += dot8(v[u], __ldg(reinterpret_cast<const uint4*>(x + m * ldx + (c + 32 * u) * 8)));
         }
     }
     for (; c < nch; c += 32) {
         const uint4 v = ld_stream(w + c * 8);
-        float f[8];
-        bf16x8_to_f32(v, f);
-        const int k = c * 8;
 #pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            if (m < M) {
-                const float4 x0 = *reinterpret_cast<const float4*>(xs + m * K + k);
-                const float4 x1 = *reinterpret_cast<const float4*>(xs + m * K + k + 4);
-                acc[m] += f[0] * x0.x + f[1] * x0.y + f[2] * x0.z + f[3] * x0.w + f[4] * x1.x + f[5] * x1.y +
-                          f[6] * x1.z + f[7] * x1.w;
-            }
-        }
+        for (int m = 0; m < MT; ++m) acc[m] += dot8(v, __ldg(reinterpret_cast<const uint4*>(x + m * ldx + c * 8)));
     }
 }
 
-// x [M][K] bf16 (row stride lda) -> shared fp32 [M][K]
-__device__ __forceinline__ void stage_input(float* xs, const bf16* x, int M, int K, long long lda) {
-    for (int i = threadIdx.x; i < M * (K / 8); i += GV_THREADS) {
-        const int m = i / (K / 8), c = i % (K / 8);
-        const uint4 v = *reinterpret_cast<const uint4*>(x + m * lda + c * 8);
-        float f[8];
-        bf16x8_to_f32(v, f);
-        float4* d = reinterpret_cast<float4*>(xs + m * K + c * 8);
-        d[0] = make_float4(f[0], f[1], f[2], f[3]);
-        d[1] = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    __syncthreads();
-}
-
-template <int MAXM, int EPI>
+template <int MT, int EPI>
 __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
-    extern __shared__ __align__(16) float gv_xs[];
-    stage_input(gv_xs, (const bf16*)g.A, g.M, g.K, g.lda);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gw = blockIdx.x * GV_WARPS + warp, nw = gridDim.x * GV_WARPS;
     const bf16* W = (const bf16*)g.W;
+    const bf16* X = (const bf16*)g.A;
     if (EPI == EPI_SWIGLU) {
-        // work item = one output column of U: gate row and up row of its group
-        const int n_out = g.N / 2;  // per shard
+        const int n_out = g.N / 2;  // U columns per shard
         const int items = g.shards * n_out;
         for (int it = gw; it < items; it += nw) {
             const int s = it / n_out, j = it % n_out;
             const int grp = j / g.granule, w = j % g.granule;
             const long long gate_row = (long long)s * g.N + grp * 2 * g.granule + w;
-            float ag[MAXM], au[MAXM];
+            float ag[MT], au[MT];
 #pragma unroll
-            for (int m = 0; m < MAXM; ++m) ag[m] = au[m] = 0.f;
-            row_dots<MAXM>(W + gate_row * g.K, gv_xs, g.K, g.M, ag);
-            row_dots<MAXM>(W + (gate_row + g.granule) * g.K, gv_xs, g.K, g.M, au);
+            for (int m = 0; m < MT; ++m) ag[m] = au[m] = 0.f;
+            row_dots<MT>(W + gate_row * g.K, X, g.lda, g.K, ag);
+            row_dots<MT>(W + (gate_row + g.granule) * g.K, X, g.lda, g.K, au);
 #pragma unroll
-            for (int m = 0; m < MAXM; ++m) {
-                if (m < g.M) {
-                    const float gs = warp_sum(ag[m]), us = warp_sum(au[m]);
-                    if (lane == 0)
-                        ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + j] = __float2bfloat16_rn(silu(gs) * us);
-                }
+            for (int m = 0; m < MT; ++m) {
+                const float gs = warp_sum(ag[m]), us = warp_sum(au[m]);
+                if (lane == 0)
+                    ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + j] = __float2bfloat16_rn(silu(gs) * us);
             }
         }
     } else {
         const int items = g.shards * g.N;
         for (int it = gw; it < items; it += nw) {
             const int s = it / g.N, n = it % g.N;
-            float acc[MAXM];
+            float acc[MT];
 #pragma unroll
-            for (int m = 0; m < MAXM; ++m) acc[m] = 0.f;
-            row_dots<MAXM>(W + (long long)it * g.K, gv_xs, g.K, g.M, acc);
+            for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+            row_dots<MT>(W + (long long)it * g.K, X, g.lda, g.K, acc);
 #pragma unroll
-            for (int m = 0; m < MAXM; ++m) {
-                if (m < g.M) {
-                    float v = warp_sum(acc[m]);
-                    if (EPI == EPI_GELU) v = gelu_erf(v);
-                    if (lane == 0) ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + n] = __float2bfloat16_rn(v);
-                }
+            for (int m = 0; m < MT; ++m) {
+                float v = warp_sum(acc[m]);
+                if (EPI == EPI_GELU) v = gelu_erf(v);
+                if (lane == 0) ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + n] = __float2bfloat16_rn(v);
             }
         }
     }
 }
 
 // row-parallel: out[m][n] = residual + sum_s <A_s[m][:], W_s[n][:]>
-template <int MAXM>
+template <int MT>
 __global__ void __launch_bounds__(GV_THREADS) gemv_row_k(GemvArgs g) {
-    extern __shared__ __align__(16) float gv_xs[];
-    // stage all shards' inputs: [shard][M][K]
-    for (int s = 0; s < g.shards; ++s) {
-        const bf16* a = (const bf16*)g.A + s * g.a_shard;
-        for (int i = threadIdx.x; i < g.M * (g.K / 8); i += GV_THREADS) {
-            const int m = i / (g.K / 8), c = i % (g.K / 8);
-            const uint4 v = *reinterpret_cast<const uint4*>(a + m * (long long)g.lda + c * 8);
-            float f[8];
-            bf16x8_to_f32(v, f);
-            float4* d = reinterpret_cast<float4*>(gv_xs + ((long long)s * g.M + m) * g.K + c * 8);
-            d[0] = make_float4(f[0], f[1], f[2], f[3]);
-            d[1] = make_float4(f[4], f[5], f[6], f[7]);
-        }
-    }
-    __syncthreads();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gw = blockIdx.x * GV_WARPS + warp, nw = gridDim.x * GV_WARPS;
     const bf16* W = (const bf16*)g.W;
+    const bf16* A = (const bf16*)g.A;
     for (int n = gw; n < g.N; n += nw) {
-        float acc[MAXM];
+        float acc[MT];
 #pragma unroll
-        for (int m = 0; m < MAXM; ++m) acc[m] = 0.f;
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
         for (int s = 0; s < g.shards; ++s)  // shard order: the fused all-reduce
-            row_dots<MAXM>(W + s * g.w_shard + (long long)n * g.K, gv_xs + (long long)s * g.M * g.K, g.K, g.M, acc);
+            row_dots<MT>(W + s * g.w_shard + (long long)n * g.K, A + s * g.a_shard, g.lda, g.K, acc);
 #pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            if (m < g.M) {
-                float v = warp_sum(acc[m]);
-                if (lane == 0) {
-                    const long long o = (long long)m * g.ldo + n;
-                    if (g.residual)
-                        v += g.residual_f32 ? ((const float*)g.residual)[o] : __bfloat162float(((const bf16*)g.residual)[o]);
-                    ((float*)g.out)[o] = v;
-                    if (g.out2) ((bf16*)g.out2)[o] = __float2bfloat16_rn(v);
-                }
+        for (int m = 0; m < MT; ++m) {
+            float v = warp_sum(acc[m]);
+            if (lane == 0) {
+                const long long o = (long long)m * g.ldo + n;
+                if (g.residual)
+                    v += g.residual_f32 ? ((const float*)g.residual)[o] : __bfloat162float(((const bf16*)g.residual)[o]);
+                ((float*)g.out)[o] = v;
+                if (g.out2) ((bf16*)g.out2)[o] = __float2bfloat16_rn(v);
             }
         }
     }
@@ -206,47 +160,41 @@ int sm_count_dev() {
     return n[dev] > 0 ? n[dev] : 148;
 }
 
-template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes, bool& done) {
-    if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) done = true;
-    return e;
+template <int MT>
+cudaError_t gemv_launch(const GemvArgs& g, cudaStream_t st) {
+    const int items = g.reduce ? g.N : g.shards * (g.epi == EPI_SWIGLU ? g.N / 2 : g.N);
+    int blocks = (items + GV_WARPS - 1) / GV_WARPS;
+    const int cap = sm_count_dev() * 16;
+    if (blocks > cap) blocks = cap;
+    if (g.reduce)
+        gemv_row_k<MT><<<blocks, GV_THREADS, 0, st>>>(g);
+    else if (g.epi == EPI_SWIGLU)
+        gemv_col_k<MT, EPI_SWIGLU><<<blocks, GV_THREADS, 0, st>>>(g);
+    else if (g.epi == EPI_GELU)
+        gemv_col_k<MT, EPI_GELU><<<blocks, GV_THREADS, 0, st>>>(g);
+    else
+        gemv_col_k<MT, EPI_STORE><<<blocks, GV_THREADS, 0, st>>>(g);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t gemv_smem_bytes(const GemvArgs& g) {
-    return (size_t)(g.reduce ? g.shards : 1) * g.M * g.K * sizeof(float);
-}
-
 bool gemv_supported(const GemvArgs& g) {
-    return g.M >= 1 && g.M <= GEMV_MAX_M && g.K % 8 == 0 && g.lda % 8 == 0 && gemv_smem_bytes(g) <= 200 * 1024 &&
+    return g.M >= 1 && g.M <= GEMV_MAX_M && g.K % 8 == 0 && g.lda % 8 == 0 &&
            (g.epi != EPI_SWIGLU || (g.N % (2 * g.granule) == 0));
 }
 
 cudaError_t gemv(const GemvArgs& g, cudaStream_t st) {
-    const size_t smem = gemv_smem_bytes(g);
-    const int items = g.reduce ? g.N : g.shards * (g.epi == EPI_SWIGLU ? g.N / 2 : g.N);
-    int blocks = (items + GV_WARPS - 1) / GV_WARPS;
-    const int cap = sm_count_dev() * 8;
-    if (blocks > cap) blocks = cap;
-    static bool a0 = false, a1 = false, a2 = false, a3 = false;
-    cudaError_t e;
-    if (g.reduce) {
-        if ((e = set_smem(gemv_row_k<GEMV_MAX_M>, 200 * 1024, a0)) != cudaSuccess) return e;
-        gemv_row_k<GEMV_MAX_M><<<blocks, GV_THREADS, smem, st>>>(g);
-    } else if (g.epi == EPI_SWIGLU) {
-        if ((e = set_smem(gemv_col_k<GEMV_MAX_M, EPI_SWIGLU>, 200 * 1024, a1)) != cudaSuccess) return e;
-        gemv_col_k<GEMV_MAX_M, EPI_SWIGLU><<<blocks, GV_THREADS, smem, st>>>(g);
-    } else if (g.epi == EPI_GELU) {
-        if ((e = set_smem(gemv_col_k<GEMV_MAX_M, EPI_GELU>, 200 * 1024, a2)) != cudaSuccess) return e;
-        gemv_col_k<GEMV_MAX_M, EPI_GELU><<<blocks, GV_THREADS, smem, st>>>(g);
-    } else {
-        if ((e = set_smem(gemv_col_k<GEMV_MAX_M, EPI_STORE>, 200 * 1024, a3)) != cudaSuccess) return e;
-        gemv_col_k<GEMV_MAX_M, EPI_STORE><<<blocks, GV_THREADS, smem, st>>>(g);
+    switch (g.M) {
+        case 1: return gemv_launch<1>(g, st);
+        case 2: return gemv_launch<2>(g, st);
+        case 3: return gemv_launch<3>(g, st);
+        case 4: return gemv_launch<4>(g, st);
+        case 5: return gemv_launch<5>(g, st);
+        case 6: return gemv_launch<6>(g, st);
+        case 7: return gemv_launch<7>(g, st);
+        default: return gemv_launch<8>(g, st);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace tpk

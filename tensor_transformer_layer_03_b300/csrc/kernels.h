@@ -82,7 +82,6 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st);
 typedef TcGemm GemvArgs;
 constexpr int GEMV_MAX_M = 8;
 bool gemv_supported(const GemvArgs& g);
-size_t gemv_smem_bytes(const GemvArgs& g);
 cudaError_t gemv(const GemvArgs& g, cudaStream_t st);
 
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
