@@ -1,281 +1,478 @@
-// Prefill attention on the tensor cores (bf16 in, fp32 softmax/accumulate).
+// Prefill attention on the 5th-generation tensor cores (bf16 in, fp32
+// softmax and accumulation), for sm_103a.
 //
-// Per shard, head and 64-query tile: O = softmax(Q K^T / sqrt(d_head) + mask) V
+// Per shard, head and query tile: O = softmax(Q K^T / sqrt(d_head) + mask) V
 // with the online (running max / running sum) softmax, so the T x T score
-// matrix never leaves registers.  Heads are independent, so every (sequence,
-// head) pair is separate work and no shard talks to another
-// (undercodenews.com/?p=110319, "the Original": each GPU computes attention
-// locally for its heads).
+// matrix never reaches memory.  Heads are independent: no shard talks to
+// another (undercodenews.com/?p=110319, "the Original": each GPU computes
+// attention locally for its heads).
 //
-// CTA = 4 warps, 16 query rows per warp, 64 keys per step.  Q stays in
-// registers; K and V tiles are double-buffered in shared memory with
-// cp.async (16-byte chunks, XOR-swizzled rows so ldmatrix is conflict-free).
-// S = Q K^T and O += P V use mma.sync m16n8k16 (bf16 x bf16 -> fp32); the
-// row max and row sum are reduced across each quad of lanes with warp
-// shuffles; P is re-packed from the S accumulators into the A operand of the
-// P V product without touching shared memory.
+// One CTA = one (sequence, head) and two 128-row query tiles that take turns
+// on the tensor core, 320 threads:
+//   warp 0     TMA producer: both Q tiles once, then K_j, V_j (128 keys x
+//              d_head, 128-byte swizzle) into a 3-slot shared-memory ring;
+//   warp 1     TMEM allocator and MMA issuer (one thread):
+//                S_t  = Q_t K_j^T          (M 128, N 128 keys, K = d_head)
+//                O_t += P_t V_j            (M 128, N = d_head, K = 128 keys;
+//                                           V read MN-major straight from the
+//                                           TMA tile, no transpose)
+//              issued in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
+//              the tensor core works on one tile while the other's softmax
+//              runs;
+//   warps 2-5  softmax of tile 0, warps 6-9 softmax of tile 1: one thread per
+//              query row (its TMEM lane) loads the row of S, applies scale and
+//              mask, updates the running max, rescales its O row in TMEM when
+//              the max grew by more than 2^8 (otherwise the stale max is kept;
+//              the factor cancels in O / l), writes P = 2^(s - m) as bf16 into
+//              a swizzled shared tile (the A operand of the next MMA) and adds
+//              P to its running sum; at the end it normalises O by the sum and
+//              stores the bf16 row.
+// TMEM: S_0 at column 0, S_1 at 128, O_0 at 256, O_1 at 256 + d_head.
+// Every mbarrier wait is bounded (2 s of %globaltimer): on expiry the kernel
+// records a device error, raises a CTA abort flag, drains its MMAs and frees
+// TMEM before returning.
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace tpk {
 
 namespace {
 
-constexpr int FA_BM = 64, FA_BN = 64, FA_THREADS = 128;
+using namespace ptx;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+constexpr int AT_ROWS = 128;   // query rows per tile (MMA M)
+constexpr int AT_KEYS = 128;   // keys per step (MMA N of S, K of P V)
+constexpr int AT_SLOTS = 3;    // K/V ring slots
+constexpr int AT_THREADS = 320;
+constexpr int HALF_BYTES = 128 * 64 * 2;  // one 128-row x 64-column swizzled half tile
+constexpr float RESCALE_LOG2 = 8.0f;      // rescale O only when the max grows by > 2^8
+constexpr unsigned long long AT_TIMEOUT_NS = 2000000000ull;
 
-// 16-byte async copy global -> shared; src_bytes == 0 fills zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// byte offset of 16-byte chunk c of row r in a [rows][D] bf16 tile
 template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
+struct Cfg {
+    static constexpr int TILE = 128 * D * 2;  // a Q, K or V tile: D/64 halves
+    static constexpr int P_TILE = 128 * AT_KEYS * 2;
+    static constexpr int Q_OFF = 0;
+    static constexpr int RING_OFF = Q_OFF + 2 * TILE;
+    static constexpr int P_OFF = RING_OFF + AT_SLOTS * TILE;
+    static constexpr int BAR_OFF = P_OFF + 2 * P_TILE;
+    static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+struct Params {
+    int n_pairs;          // pairs of query tiles per (sequence, head)
+    int H, B, hl, Tq, pos, causal, nkeys;
+    int cached;           // K/V from the cache maps (else from the QKV buffer)
+    float scale_log2;     // softmax scale * log2(e)
+    bf16* out;            // [tp][B*Tq][hl*D]
+    long long out_shard;
+    int out_ld;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// rows [r0, r0+ROWS) of a [rows][D] matrix with row stride `ld` (elements)
-// into a swizzled tile; rows >= nrows are zero-filled.
-template <int D, int ROWS>
-__device__ __forceinline__ void load_tile(uint32_t s_base, const bf16* g, long long ld, int r0, int nrows) {
-    constexpr int CH = D / 8;  // 16-byte chunks per row
-    for (int i = threadIdx.x; i < ROWS * CH; i += FA_THREADS) {
-        const int r = i / CH, c = i % CH;
-        const int row = r0 + r;
-        const bool ok = row < nrows;
-        const bf16* src = g + (ok ? (long long)row * ld : 0) + c * 8;
-        cp_async16(s_base + swz<D>(r, c), src, ok ? 16 : 0);
-    }
+// K-major operand: `bytes` into the tile along K (a multiple of 32 below 128
+// selects the 16-element K step inside the swizzle row; 64-column halves
+// follow each other HALF_BYTES apart).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int k_elem) {
+    return sw128_desc(tile + (uint32_t)(k_elem / 64) * HALF_BYTES + (uint32_t)(k_elem % 64) * 2, 16, 1024);
 }
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(FA_THREADS) flash_fwd_k(AttnArgs a) {
-    extern __shared__ __align__(128) uint8_t fa_smem[];
-    constexpr int TILE_BYTES = FA_BN * D * 2;
-    const uint32_t sQ = smem_addr(fa_smem);
-    const uint32_t sK = sQ + FA_BM * D * 2;        // 2 buffers
-    const uint32_t sV = sK + 2 * TILE_BYTES;        // 2 buffers
+template <int D>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, Params p) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* q_full = bars;                 // 1
+    uint64_t* kv_full = bars + 1;            // AT_SLOTS
+    uint64_t* kv_empty = kv_full + AT_SLOTS; // AT_SLOTS
+    uint64_t* s_full = kv_empty + AT_SLOTS;  // 2
+    uint64_t* p_full = s_full + 2;           // 2
+    uint64_t* o_full = p_full + 2;           // 2
+    uint64_t* drain = o_full + 2;            // 1
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    const int qtile = gridDim.x - 1 - blockIdx.x;  // longest (causal) tiles first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int s = h / a.hl, jl = h % a.hl;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int g = lane / 4, t4 = lane % 4;
-    const long long M = (long long)a.B * a.Tq;
-    const int rowlen = 3 * a.hl * D;
-    const bf16* base = (const bf16*)a.qkv + s * M * rowlen + (long long)b * a.Tq * rowlen;
-    const bf16* Qg = base + jl * D;
-    const bf16 *Kg, *Vg;
-    long long kv_ld;
-    if (a.kc) {
-        Kg = (const bf16*)a.kc + ((long long)b * a.H + h) * a.cap * D;
-        Vg = (const bf16*)a.vc + ((long long)b * a.H + h) * a.cap * D;
-        kv_ld = D;
-    } else {
-        Kg = base + a.hl * D + jl * D;
-        Vg = base + 2 * a.hl * D + jl * D;
-        kv_ld = rowlen;
+    const int hb = p.H * p.B;
+    const int pair = p.n_pairs - 1 - (int)(blockIdx.x / hb);  // longest (causal) work first
+    const int head = (int)(blockIdx.x % hb) % p.H;
+    const int b = (int)(blockIdx.x % hb) / p.H;
+    const int s = head / p.hl, jl = head % p.hl;
+
+    // query tile t covers rows q0(t) .. q0(t)+127 of the sequence and needs
+    // key tiles 0 .. nkt(t)-1
+    auto q0 = [&](int t) { return pair * 2 * AT_ROWS + t * AT_ROWS; };
+    auto nkt = [&](int t) {
+        if (q0(t) >= p.Tq) return 0;
+        const int kmax = p.causal ? min(p.nkeys, p.pos + q0(t) + AT_ROWS) : p.nkeys;
+        return (kmax + AT_KEYS - 1) / AT_KEYS;
+    };
+    const bool valid1 = q0(1) < p.Tq;
+    const int n_kt = nkt(valid1 ? 1 : 0);  // key tiles loaded (tile 1 needs every one of them)
+    const int last_t = valid1 ? 1 : 0;     // the last tile to use each K_j / V_j
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < AT_SLOTS; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 4);
+            mbar_init(&o_full[t], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
     }
-    const int q0 = qtile * FA_BM;
-    const int nkeys = a.pos + a.Tq;
-    const int kmax = CAUSAL ? min(nkeys, a.pos + q0 + FA_BM) : nkeys;
-    const int n_kt = (kmax + FA_BN - 1) / FA_BN;
+    if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t sQ = smem_u32(smem + C::Q_OFF);
+    const uint32_t sRing = smem_u32(smem + C::RING_OFF);
+    const uint32_t sP = smem_u32(smem + C::P_OFF);
 
-    load_tile<D, FA_BM>(sQ, Qg, rowlen, q0, a.Tq);
-    load_tile<D, FA_BN>(sK, Kg, kv_ld, 0, kmax);
-    load_tile<D, FA_BN>(sV, Vg, kv_ld, 0, kmax);
-    cp_async_commit();
+    // column of head jl's Q / K / V in a QKV row, and the map coordinates
+    const int rowq = jl * D;
+    const int c2 = p.cached ? head : b;
+    const int c3 = p.cached ? b : s;
+    const int kcol = p.cached ? 0 : (p.hl + jl) * D;
+    const int vcol = p.cached ? 0 : (2 * p.hl + jl) * D;
 
-    // scores are kept in log2 units: x = s * scale * log2(e)
-    const float sl2 = a.scale * 1.4426950408889634f;
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    uint32_t qf[D / 16][4];
-    const int qrow_base = a.pos + q0 + warp * 16;  // absolute position of the warp's first row
-
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < n_kt) {
-            load_tile<D, FA_BN>(sK + (buf ^ 1) * TILE_BYTES, Kg, kv_ld, (kt + 1) * FA_BN, kmax);
-            load_tile<D, FA_BN>(sV + (buf ^ 1) * TILE_BYTES, Vg, kv_ld, (kt + 1) * FA_BN, kmax);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        if (kt == 0) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int r = warp * 16 + (lane % 8) + ((lane / 8) % 2) * 8;
-                const int c = kk * 2 + lane / 16;
-                ldsm_x4(sQ + swz<D>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            mbar_expect_tx(q_full, (valid1 ? 2 : 1) * C::TILE);
+            for (int t = 0; t < (valid1 ? 2 : 1); ++t) {
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_4d(sQ + t * C::TILE + h * HALF_BYTES, &tmQ, smem_u32(q_full), rowq + h * 64, q0(t), b,
+                                s);
             }
-        }
-        const uint32_t kb = sK + buf * TILE_BYTES, vb = sV + buf * TILE_BYTES;
-        // S = Q K^T for 16 rows x 64 keys
-        float sc[FA_BN / 8][4];
-#pragma unroll
-        for (int i = 0; i < FA_BN / 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-            for (int np = 0; np < FA_BN / 16; ++np) {
-                uint32_t b0, b1, b2, b3;
-                const int r = np * 16 + (lane % 8) + (lane / 16) * 8;
-                const int c = kk * 2 + (lane / 8) % 2;
-                ldsm_x4(kb + swz<D>(r, c), b0, b1, b2, b3);
-                mma_bf16(sc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-                mma_bf16(sc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
-            }
-        }
-        // mask (causal diagonal tiles and the ragged key tail), running max
-        const int k0 = kt * FA_BN;
-        const bool need_mask = (k0 + FA_BN > kmax) || (CAUSAL && k0 + FA_BN - 1 > qrow_base);
-        float mx[2] = {mrow[0], mrow[1]};
-#pragma unroll
-        for (int i = 0; i < FA_BN / 8; ++i) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float x = sc[i][e] * sl2;
-                if (need_mask) {
-                    const int key = k0 + i * 8 + 2 * t4 + (e & 1);
-                    const int qpos = qrow_base + g + (e >> 1) * 8;
-                    if (key >= kmax || (CAUSAL && key > qpos)) x = -INFINITY;
+            for (int i = 0; i < 2 * n_kt && ok; ++i) {
+                const int slot = i % AT_SLOTS;
+                const uint32_t ph = (uint32_t)(i / AT_SLOTS) & 1u;
+                if (!mbar_wait(&kv_empty[slot], ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
                 }
-                sc[i][e] = x;
-                mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                const int j = i >> 1;
+                const bool is_v = i & 1;
+                const CUtensorMap* map = is_v ? &tmV : &tmK;
+                const int col = is_v ? vcol : kcol;
+                mbar_expect_tx(&kv_full[slot], C::TILE);
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_4d(sRing + slot * C::TILE + h * HALF_BYTES, map, smem_u32(&kv_full[slot]), col + h * 64,
+                                j * AT_KEYS, c2, c3);
+            }
+            if (!ok) {
+                const unsigned long long t0 = globaltimer();
+                while (globaltimer() - t0 < 1000000ull) __nanosleep(1000);
             }
         }
-        float corr[2];
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(AT_ROWS, AT_KEYS, false);
+            constexpr uint32_t IDESC_O = idesc_bf16(AT_ROWS, D, true);
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.err, p.timeout_ns);
+            tc_fence_after();
+            int kv_seen = -1;  // ring items known to have landed
+            auto need_item = [&](int i) -> bool {
+                while (kv_seen < i) {
+                    const int n = kv_seen + 1;
+                    if (!mbar_wait(&kv_full[n % AT_SLOTS], (uint32_t)(n / AT_SLOTS) & 1u, abort_flag, p.err,
+                                   p.timeout_ns))
+                        return false;
+                    tc_fence_after();
+                    kv_seen = n;
+                }
+                return true;
+            };
+            auto issue_s = [&](int t, int j) {
+                const uint32_t ks = sRing + (uint32_t)((2 * j) % AT_SLOTS) * C::TILE;
+                const uint32_t qs = sQ + t * C::TILE;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            corr[r] = mrow[r] == -INFINITY ? 0.f : exp2f(mrow[r] - mx[r]);
-            mrow[r] = mx[r];
-        }
-        const float mb[2] = {mx[0] == -INFINITY ? 0.f : mx[0], mx[1] == -INFINITY ? 0.f : mx[1]};
-        float rs[2] = {0.f, 0.f};
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_f16(tmem_base + t * AT_KEYS, kmajor_desc(qs, kk * 16), kmajor_desc(ks, kk * 16), IDESC_S,
+                             kk > 0 ? 1u : 0u);
+                umma_commit(&s_full[t]);
+                if (t == last_t) umma_commit(&kv_empty[(2 * j) % AT_SLOTS]);
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t vs = sRing + (uint32_t)((2 * j + 1) % AT_SLOTS) * C::TILE;
+                const uint32_t ps = sP + t * C::P_TILE;
+                const uint32_t o_t = tmem_base + 2 * AT_KEYS + t * D;
 #pragma unroll
-        for (int i = 0; i < FA_BN / 8; ++i) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p = exp2f(sc[i][e] - mb[e >> 1]);
-                sc[i][e] = p;
-                rs[e >> 1] += p;
+                for (int kk = 0; kk < AT_KEYS / 16; ++kk)
+                    umma_f16(o_t, kmajor_desc(ps, kk * 16), sw128_desc(vs + kk * 16 * 128, HALF_BYTES, 1024), IDESC_O,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+                if (t == last_t) umma_commit(&kv_empty[(2 * j + 1) % AT_SLOTS]);
+                if (j == nkt(t) - 1) umma_commit(&o_full[t]);
+            };
+            if (ok && n_kt > 0) {
+                ok = need_item(0);
+                for (int t = 0; t < 2 && ok; ++t)
+                    if (nkt(t) > 0) issue_s(t, 0);
+            }
+            for (int j = 0; j < n_kt && ok; ++j) {
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j < nkt(t)) {
+                        if (!need_item(2 * j + 1) ||
+                            !mbar_wait(&p_full[t], (uint32_t)j & 1u, abort_flag, p.err, p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, j);
+                    }
+                    if (j + 1 < nkt(t)) {
+                        if (!need_item(2 * (j + 1))) {
+                            ok = false;
+                            break;
+                        }
+                        issue_s(t, j + 1);
+                    }
+                }
+            }
+            // drain: every MMA issued here completes before TMEM is freed
+            umma_commit(drain);
+            const uint32_t a = smem_u32(drain);
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(a, 0)) {
+                if (globaltimer() - t0 > p.timeout_ns) {
+                    record_error(p.err, DEV_ERR_TIMEOUT);
+                    break;
+                }
             }
         }
+    } else {
+        // softmax warps: tile t, TMEM lane quarter q (a warp may only touch
+        // lanes 32*(warp % 4) .. +31)
+        const int t = (warp - 2) / 4;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // row of the tile = TMEM lane
+        const int q0t = q0(t), nkt_t = nkt(t);
+        if (nkt_t > 0) {
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const uint32_t tS = tmem_base + lane_off + t * AT_KEYS;
+            const uint32_t tO = tmem_base + lane_off + 2 * AT_KEYS + t * D;
+            const int qpos = p.pos + q0t + row;          // absolute position of this query
+            const int warp_qmin = p.pos + q0t + quarter * 32;
+            const uint32_t prow = sP + t * C::P_TILE + row * 128;
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nkt_t; ++j) {
+                if (!mbar_wait_warp(&s_full[t], (uint32_t)j & 1u, abort_flag, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float sv[AT_KEYS];
+                {
+                    uint32_t r[4][32];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) lrow[r] = lrow[r] * corr[r] + rs[r];
+                    for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + 32 * c, r[c]);
+                    tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= corr[0];
-            o[i][1] *= corr[0];
-            o[i][2] *= corr[1];
-            o[i][3] *= corr[1];
-        }
-        // O += P V: P's accumulator layout is the A-operand layout of the next mma
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int kk = 0; kk < FA_BN / 16; ++kk) {
-            const uint32_t a0 = pack2(sc[2 * kk][0], sc[2 * kk][1]);
-            const uint32_t a1 = pack2(sc[2 * kk][2], sc[2 * kk][3]);
-            const uint32_t a2 = pack2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-            const uint32_t a3 = pack2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                        for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(r[c][i]) * p.scale_log2;
+                }
+                const int k0 = j * AT_KEYS;
+                const bool masked = (k0 + AT_KEYS > p.nkeys) || (p.causal && k0 + AT_KEYS - 1 > warp_qmin);
+                if (masked) {
+                    const int lim = p.causal ? min(p.nkeys - 1, qpos) : p.nkeys - 1;  // last visible key
 #pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                uint32_t b0, b1, b2, b3;
-                const int r = kk * 16 + (lane % 8) + ((lane / 8) % 2) * 8;
-                const int c = np * 2 + lane / 16;
-                ldsm_x4_t(vb + swz<D>(r, c), b0, b1, b2, b3);
-                mma_bf16(o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                    for (int i = 0; i < AT_KEYS; ++i)
+                        if (k0 + i > lim) sv[i] = -INFINITY;
+                }
+                float mx = sv[0];
+#pragma unroll
+                for (int i = 1; i < AT_KEYS; ++i) mx = fmaxf(mx, sv[i]);
+                // keep the stale max unless the row max grew by more than 2^8
+                const bool grow = j == 0 || mx > m_used + RESCALE_LOG2;
+                const float m_new = grow ? fmaxf(m_used, mx) : m_used;
+                if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                    const float corr = grow ? ex2(m_used - m_new) : 1.f;
+                    l *= corr;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float ov[32];
+                        tmem_ld32(tO + 32 * c, ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] *= corr;
+                        tmem_st32(tO + 32 * c, ov);
+                    }
+                    tmem_st_wait();
+                }
+                m_used = m_new;
+                const float mb = m_used == -INFINITY ? 0.f : m_used;
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < AT_KEYS / 8; ++c) {
+                    float e[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        e[i] = ex2(sv[8 * c + i] - mb);
+                        rs += e[i];
+                    }
+                    const uint4 v = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                                               pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+                    const int half = c / 8, chunk = c % 8;
+                    const uint32_t addr = prow + half * HALF_BYTES + (uint32_t)((chunk ^ (row & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                                 "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                l += rs;
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[t]);
+            }
+            if (ok && mbar_wait_warp(&o_full[t], 0, abort_flag, p.err, p.timeout_ns)) {
+                tc_fence_after();
+                const float inv = 1.f / l;
+                const bool row_ok = q0t + row < p.Tq;
+                bf16* dst = p.out + s * p.out_shard + ((long long)b * p.Tq + q0t + row) * p.out_ld + jl * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float ov[32];
+                    tmem_ld32(tO + 32 * c, ov);
+                    if (row_ok) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_uint4(pack_bf16x2(ov[8 * q] * inv, ov[8 * q + 1] * inv),
+                                               pack_bf16x2(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
+                                               pack_bf16x2(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
+                                               pack_bf16x2(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+                    }
+                }
             }
         }
-        __syncthreads();  // the buffer is refilled by the next iteration's loads
     }
-    // finish: row sums across the quad, normalise, store bf16
-    float inv[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        float l = lrow[r];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        inv[r] = 1.f / l;
-    }
-    bf16* out = (bf16*)a.out + s * M * (a.hl * D) + (long long)b * a.Tq * (a.hl * D) + jl * D;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int t = q0 + warp * 16 + g + r * 8;
-        if (t < a.Tq) {
-            uint32_t* dst = reinterpret_cast<uint32_t*>(out + (long long)t * (a.hl * D));
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) dst[i * 4 + t4] = pack2(o[i][2 * r] * inv[r], o[i][2 * r + 1] * inv[r]);
-        }
-    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int D, bool CAUSAL>
-cudaError_t flash_launch(const AttnArgs& a, cudaStream_t st) {
-    constexpr int SMEM = FA_BM * D * 2 + 4 * FA_BN * D * 2;
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    }
+    return fn;
+}
+
+// 4-D bf16 tensor [d3][d2][d1][d0] (d0 contiguous), box {64, 128, 1, 1},
+// 128-byte swizzle; reads outside the tensor fill zeros.
+bool make_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4], const uint64_t (&strides_bytes)[3]) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    cuuint64_t st[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, st, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t attn_launch(const AttnArgs& a, int* dev_err, cudaStream_t st) {
+    using C = Cfg<D>;
     static bool attr[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(flash_fwd_k<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr[dev] = true;
     }
-    dim3 grid((a.Tq + FA_BM - 1) / FA_BM, a.H, a.B);
-    flash_fwd_k<D, CAUSAL><<<grid, FA_THREADS, SMEM, st>>>(a);
+    const uint64_t rowlen = 3ull * a.hl * D;
+    const uint64_t M = (uint64_t)a.B * a.Tq;
+    CUtensorMap mq, mk, mv;
+    // QKV buffer viewed as [tp][B][Tq][3*hl*D]
+    const uint64_t qdims[4] = {rowlen, (uint64_t)a.Tq, (uint64_t)a.B, (uint64_t)(a.H / a.hl)};
+    const uint64_t qstr[3] = {rowlen * 2, (uint64_t)a.Tq * rowlen * 2, M * rowlen * 2};
+    if (!make_map4(&mq, a.qkv, qdims, qstr)) return cudaErrorInvalidValue;
+    const int nkeys = a.pos + a.Tq;
+    if (a.kc) {
+        // cache [B][H][cap][D], cut at the last valid key so the rows past it
+        // read as zeros
+        const uint64_t kdims[4] = {(uint64_t)D, (uint64_t)nkeys, (uint64_t)a.H, (uint64_t)a.B};
+        const uint64_t kstr[3] = {(uint64_t)D * 2, (uint64_t)a.cap * D * 2, (uint64_t)a.H * a.cap * D * 2};
+        if (!make_map4(&mk, a.kc, kdims, kstr) || !make_map4(&mv, a.vc, kdims, kstr)) return cudaErrorInvalidValue;
+    } else {
+        mk = mq;
+        mv = mq;
+    }
+    Params p{};
+    p.n_pairs = (a.Tq + 2 * AT_ROWS - 1) / (2 * AT_ROWS);
+    p.H = a.H;
+    p.B = a.B;
+    p.hl = a.hl;
+    p.Tq = a.Tq;
+    p.pos = a.pos;
+    p.causal = a.causal;
+    p.nkeys = nkeys;
+    p.cached = a.kc != nullptr;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.out = (bf16*)a.out;
+    p.out_shard = (long long)M * a.hl * D;
+    p.out_ld = a.hl * D;
+    p.err = dev_err;
+    p.timeout_ns = AT_TIMEOUT_NS;
+    const long long grid = (long long)p.n_pairs * a.H * a.B;
+    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    attn_tc_kernel<D><<<(unsigned)grid, AT_THREADS, C::SMEM, st>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool tc_attention_supported(const AttnArgs& a) { return a.is_bf16 && (a.dh == 64 || a.dh == 128); }
+bool tc_attention_supported(const AttnArgs& a) {
+    // TMA needs 16-byte aligned row strides: 3*hl*dh and dh bf16 elements are
+    // multiples of 8 for dh in {64, 128}
+    return a.is_bf16 && (a.dh == 64 || a.dh == 128);
+}
 
-cudaError_t tc_attention(const AttnArgs& a, cudaStream_t st) {
-    if (a.dh == 128) return a.causal ? flash_launch<128, true>(a, st) : flash_launch<128, false>(a, st);
-    if (a.dh == 64) return a.causal ? flash_launch<64, true>(a, st) : flash_launch<64, false>(a, st);
+cudaError_t tc_attention(const AttnArgs& a, int* dev_err, cudaStream_t st) {
+    if (a.dh == 128) return attn_launch<128>(a, dev_err, st);
+    if (a.dh == 64) return attn_launch<64>(a, dev_err, st);
     return cudaErrorNotSupported;
 }
 

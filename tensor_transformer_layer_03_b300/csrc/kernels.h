@@ -86,7 +86,8 @@ cudaError_t gemv(const GemvArgs& g, cudaStream_t st);
 
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
 bool tc_attention_supported(const AttnArgs& a);
-cudaError_t tc_attention(const AttnArgs& a, cudaStream_t st);
+// dev_err: device word where bounded waits record a timeout
+cudaError_t tc_attention(const AttnArgs& a, int* dev_err, cudaStream_t st);
 
 // ---- single-token decode (decode.cu) ------------------------------------------
 // Split-KV attention: partial (max, sum, output) per key chunk in `scratch`

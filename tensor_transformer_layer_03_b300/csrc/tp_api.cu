@@ -323,7 +323,7 @@ tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int
     if (split_kv) {
         e = tpk::decode_attention(a, static_cast<float*>(scratch), st);
     } else if (a.is_bf16 && tpk::tc_attention_supported(a)) {
-        e = tpk::tc_attention(a, st);
+        e = tpk::tc_attention(a, device_error_word(), st);
     } else {
         e = tpk::simt_attention(a, st);
     }

@@ -133,6 +133,10 @@ ATTN_CASES = [
     (256, 4, 1, 1, 1, True, 1.0),
     (256, 8, 2, 3, 64, True, 2.0),   # d_head 32
     (4096, 32, 4, 1, 512, True, 1.0),
+    # several 128-key steps with large scores: the running max grows by more
+    # than 2^8 between steps, so the output rows are rescaled in flight
+    (1024, 8, 2, 1, 700, True, 4.0),
+    (512, 8, 4, 2, 300, False, 4.0),   # d_head 64, no mask, ragged tail
 ]
 
 
@@ -165,6 +169,7 @@ def test_attention_prefill(tp, d, H, deg, B, T, causal, qs, dtype):
     (512, 4, 4, 3, 1, 0, 8),         # first token
     (512, 8, 2, 1, 1, 9000, 9001),   # more keys than 64 chunks of 128
     (512, 4, 2, 2, 37, 50, 100),     # a chunk of tokens after a prefix
+    (1024, 8, 4, 1, 300, 200, 640),  # a longer chunk after a prefix, NaN tail
 ])
 def test_attention_with_cache(tp, d, H, deg, B, T, pos, cap, dtype):
     plan = _plan(tp, d, H, 8 * deg, deg, dtype=dtype)
@@ -174,6 +179,9 @@ def test_attention_with_cache(tp, d, H, deg, B, T, pos, cap, dtype):
     qkv = torch.stack([I.make_matrix(M, 3 * d // deg, dtype, g) for _ in range(deg)])
     kc = torch.randn(B, H, cap, dh, generator=g).to(I.torch_dtype(dtype))
     vc = torch.randn(B, H, cap, dh, generator=g).to(I.torch_dtype(dtype))
+    # cache rows past the last key are never read: fill them with NaN
+    kc[:, :, pos + T:] = float("nan")
+    vc[:, :, pos + T:] = float("nan")
     kc_d, vc_d = kc.to(DEV), vc.to(DEV)
     out = torch.empty(deg, M, d // deg, dtype=I.torch_dtype(dtype), device=DEV)
     nscr = plan.attention_scratch_bytes(B, T, cap)
@@ -196,4 +204,4 @@ def test_attention_with_cache(tp, d, H, deg, B, T, pos, cap, dtype):
         new = k[b * T:(b + 1) * T].reshape(T, H, dh).transpose(1, 0, 2)
         assert np.array_equal(kn[b, :, pos:pos + T], new)
         assert np.array_equal(kn[b, :, :pos], np64(kc[b, :, :pos]))
-        assert np.array_equal(kn[b, :, pos + T:], np64(kc[b, :, pos + T:]))
+        assert np.array_equal(kn[b, :, pos + T:], np64(kc[b, :, pos + T:]), equal_nan=True)
