@@ -11,18 +11,26 @@
 //       -- every shard's partial product is accumulated, in shard order, into
 //       the same TMEM accumulator, so no partial is ever written to memory.
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0   TMA producer: 128x64 tile of A and 256x64 tile of W per stage,
-//            128-byte swizzle, 4-stage shared-memory ring (48 KB per stage);
-//   warp 1   TMEM allocator and MMA issuer: tcgen05.mma kind::f16, M=128,
-//            N=256, K=16, into one of two 128x256 fp32 TMEM accumulators;
+// Two variants of one persistent kernel (one CTA per SM, 192 threads):
+//  * PAIR (M > 128): clusters of two CTAs on neighbouring SMs compute a
+//    256 x 256 output tile with 2-SM MMAs (tcgen05 .cta_group::2, M = 256):
+//    each CTA stages its own 128 rows of A and 128 of the 256 rows of W, the
+//    even CTA issues the MMAs, and each CTA's TMEM holds its 128 output rows.
+//    32 KB per k-block per SM, 6-stage ring.
+//  * single (M <= 128): 128 x 256 tiles on one SM, 48 KB stages, 4 deep.
+// Roles in each CTA:
+//   warp 0   TMA producer (128-byte swizzle, ring of k-blocks of 64);
+//   warp 1   TMEM allocator; in the issuing CTA also the MMA thread:
+//            tcgen05.mma kind::f16, K = 16 steps, into one of two 256-column
+//            fp32 TMEM accumulators;
 //   warps 2-5 epilogue: tcgen05.ld of the finished accumulator (each warp its
 //            32-lane quarter), activation / residual, stores to global.
 // The epilogue of tile i overlaps the main loop of tile i+1 (two TMEM
 // accumulators = all 512 columns).  Every mbarrier wait is bounded: after
 // `timeout_ns` the waiting role records TP_ERR_DEVICE_TIMEOUT's device code,
 // raises a CTA-wide abort flag and leaves its loop; in-flight tensor-core
-// work is drained and TMEM freed before the CTA exits.
+// work is drained and TMEM freed before the CTA exits, and the two CTAs of a
+// pair leave together.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -33,17 +41,23 @@ namespace tpk {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int BN = 256, BK = 64;          // output columns per tile, K per stage
+constexpr int A_ROWS = 128;                // A rows staged per CTA
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s
 
-// instruction descriptor: D fp32, A/B bf16, both K-major, M=128, N=256
-constexpr uint32_t IDESC = ptx::idesc_bf16(BM, BN, false);
+template <bool PAIR>
+struct GCfg {
+    static constexpr int TILE_M = PAIR ? 256 : 128;   // output rows per tile
+    static constexpr int W_ROWS = PAIR ? BN / 2 : BN;  // W rows staged per CTA
+    static constexpr int A_BYTES = A_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + W_ROWS * BK * 2;
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    // instruction descriptor: D fp32, A/B bf16, both K-major
+    static constexpr uint32_t IDESC = ptx::idesc_bf16(TILE_M, BN, false);
+};
 
 struct Params {
     int epi, M, N, K, shards, reduce;
@@ -76,42 +90,49 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32], 
     }
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, Params p) {
+    using C = GCfg<PAIR>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* tmem_full = empty + STAGES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tmem_full = empty + C::STAGES;
     uint64_t* tmem_empty = tmem_full + 2;
     uint64_t* drain = tmem_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // PAIR: rank in the cluster (0 issues the MMAs) and the tile stream of the pair
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int unit = PAIR ? (int)(blockIdx.x / 2) : (int)blockIdx.x;
+    const int n_units = PAIR ? (int)(gridDim.x / 2) : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
-            mbar_init(&tmem_empty[b], 4);
+            mbar_init(&tmem_empty[b], PAIR ? 8 : 4);  // epilogue warps of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_async_smem();
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (PAIR)
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        else
+            tmem_alloc(tmem_slot, TMEM_COLS);
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kb_per_tile = p.reduce ? p.shards * p.k_blocks : p.k_blocks;
@@ -121,11 +142,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+            for (int t = unit; t < p.n_tiles && ok; t += n_units) {
                 const int m_blk = t % p.m_blocks;
                 const int rest = t / p.m_blocks;
                 const int shard = p.reduce ? 0 : rest / p.n_blocks;
                 const int n_blk = p.reduce ? rest : rest % p.n_blocks;
+                const int a_row = m_blk * C::TILE_M + (int)rank * A_ROWS;
+                const int w_row = n_blk * BN + (int)rank * C::W_ROWS;
                 for (int kb = 0; kb < kb_per_tile; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
@@ -133,11 +156,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const int s = p.reduce ? kb / p.k_blocks : shard;
                     const int kk = (p.reduce ? kb % p.k_blocks : kb) * BK;
-                    uint8_t* sa = smem + stage * STAGE_BYTES;
-                    mbar_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_3d(smem_u32(sa), &tmA, smem_u32(&full[stage]), kk, m_blk * BM, p.reduce ? s : 0);
-                    tma_load_3d(smem_u32(sa + A_STAGE_BYTES), &tmW, smem_u32(&full[stage]), kk, n_blk * BN, s);
-                    if (++stage == STAGES) {
+                    const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+                    if constexpr (PAIR) {
+                        // both CTAs' copies complete on the issuing CTA's barrier
+                        const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
+                        if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                        tma_load_3d_pair(sa, &tmA, bar0, kk, a_row, p.reduce ? s : 0);
+                        tma_load_3d_pair(sa + C::A_BYTES, &tmW, bar0, kk, w_row, s);
+                    } else {
+                        mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+                        tma_load_3d(sa, &tmA, smem_u32(&full[stage]), kk, a_row, p.reduce ? s : 0);
+                        tma_load_3d(sa + C::A_BYTES, &tmW, smem_u32(&full[stage]), kk, w_row, s);
+                    }
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -150,12 +181,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int i = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++i) {
+            for (int t = unit; t < p.n_tiles && ok; t += n_units, ++i) {
                 const int buf = i & 1;
                 const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
                 if (!mbar_wait(&tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
@@ -170,23 +201,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint64_t adesc = sw128_kmajor(sa);
-                    const uint64_t bdesc = sw128_kmajor(sa + A_STAGE_BYTES);
+                    const uint64_t bdesc = sw128_kmajor(sa + C::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)  // +32 bytes per K step inside the swizzle row
-                        umma_f16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), IDESC,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(&empty[stage]);
-                    if (++stage == STAGES) {
+                    for (int k = 0; k < BK / 16; ++k) {  // +32 bytes per K step inside the swizzle row
+                        const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                        if constexpr (PAIR)
+                            umma_f16_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), C::IDESC, acc);
+                        else
+                            umma_f16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), C::IDESC, acc);
+                    }
+                    if constexpr (PAIR)
+                        umma_commit_pair(&empty[stage], 3);  // frees the stage in both CTAs
+                    else
+                        umma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) umma_commit(&tmem_full[buf]);
+                if (ok) {
+                    if constexpr (PAIR)
+                        umma_commit_pair(&tmem_full[buf], 3);
+                    else
+                        umma_commit(&tmem_full[buf]);
+                }
             }
             // drain: wait for every MMA issued by this thread before TMEM is freed
-            umma_commit(drain);
+            if constexpr (PAIR)
+                umma_commit_pair(drain, 1);
+            else
+                umma_commit(drain);
             const uint32_t a = smem_u32(drain);
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(a, 0)) {
@@ -200,7 +246,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // epilogue warps 2..5 -> TMEM lane quarters 2,3,0,1
         const int quarter = warp & 3;
         int i = 0;
-        for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++i) {
+        for (int t = unit; t < p.n_tiles; t += n_units, ++i) {
             const int buf = i & 1;
             const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
             if (!mbar_wait_warp(&tmem_full[buf], acc_phase, abort_flag, p.err, p.timeout_ns)) break;
@@ -209,7 +255,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int rest = t / p.m_blocks;
             const int shard = p.reduce ? 0 : rest / p.n_blocks;
             const int n_blk = p.reduce ? rest : rest % p.n_blocks;
-            const int row = m_blk * BM + quarter * 32 + lane;
+            const int row = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
             const int col_base = n_blk * BN;
             const bool row_ok = row < p.M;
@@ -300,16 +346,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[buf]), 0));  // the issuing CTA's
+                else
+                    mbar_arrive(&tmem_empty[buf]);
+            }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // no remote arrive or MMA write lands after the peer leaves
     tc_fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                     : "memory");
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -362,23 +416,61 @@ int sm_count() {
 
 bool tc_gemm_supported(int M, int N, int K) { return M >= 1 && N >= 1 && K >= 8 && K % 8 == 0; }
 
-cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st) {
-    static bool attr_set[64] = {false};
+namespace {
+
+// Co-resident clusters of two for the paired kernel (an SM pair must come
+// from one GPC, so this can be below SMs / 2).
+int pair_slots() {
+    static int n[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+    if (dev < 0 || dev >= 64) return 0;
+    if (!n[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * 74, 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = GCfg<true>::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true>, &cfg) != cudaSuccess || c <= 0) {
+            cudaGetLastError();
+            c = -1;
+        }
+        n[dev] = c;
     }
-    if (g.epi == EPI_SWIGLU && (g.granule != 32 || g.N % 64 != 0)) return cudaErrorNotSupported;
+    return n[dev] > 0 ? n[dev] : 0;
+}
+
+template <bool PAIR>
+cudaError_t set_smem_attr() {
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !done[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(tc_gemm_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<PAIR>::SMEM);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <bool PAIR>
+cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, cudaStream_t st) {
+    using C = GCfg<PAIR>;
     CUtensorMap tmA, tmW;
     const uint64_t a_shards = g.reduce ? (uint64_t)g.shards : 1;
     if (!make_map(&tmA, g.A, (uint64_t)g.K, (uint64_t)g.M, a_shards, (uint64_t)g.lda * 2,
-                  (uint64_t)g.M * g.lda * 2, BM))
+                  (uint64_t)g.M * g.lda * 2, A_ROWS))
         return cudaErrorInvalidValue;
     if (!make_map(&tmW, g.W, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.shards, (uint64_t)g.K * 2,
-                  (uint64_t)g.w_shard * 2, BN))
+                  (uint64_t)g.w_shard * 2, C::W_ROWS))
         return cudaErrorInvalidValue;
     Params p{};
     p.epi = g.epi;
@@ -387,7 +479,7 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st) {
     p.K = g.K;
     p.shards = g.shards;
     p.reduce = g.reduce;
-    p.m_blocks = (g.M + BM - 1) / BM;
+    p.m_blocks = (g.M + C::TILE_M - 1) / C::TILE_M;
     p.n_blocks = (g.N + BN - 1) / BN;
     p.k_blocks = (g.K + BK - 1) / BK;
     p.n_tiles = p.m_blocks * p.n_blocks * (g.reduce ? 1 : g.shards);
@@ -400,9 +492,40 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st) {
     p.granule = g.granule;
     p.err = dev_err;
     p.timeout_ns = DEFAULT_TIMEOUT_NS;
-    const int grid = p.n_tiles < sm_count() ? p.n_tiles : sm_count();
-    tc_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmW, p);
-    return cudaGetLastError();
+    const int units = p.n_tiles < slots ? p.n_tiles : slots;
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * units, 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, tmA, tmW, p);
+    } else {
+        tc_gemm_kernel<false><<<units, NUM_THREADS, C::SMEM, st>>>(tmA, tmW, p);
+        return cudaGetLastError();
+    }
+}
+
+}  // namespace
+
+cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st) {
+    if (g.epi == EPI_SWIGLU && (g.granule != 32 || g.N % 64 != 0)) return cudaErrorNotSupported;
+    cudaError_t e = set_smem_attr<false>();
+    if (e == cudaSuccess) e = set_smem_attr<true>();
+    if (e != cudaSuccess) return e;
+    // 2-SM tiles once there is more than one 128-row block of tokens
+    if (g.M > A_ROWS) {
+        const int slots = pair_slots();
+        if (slots > 0) return gemm_launch<true>(g, dev_err, slots, st);
+    }
+    return gemm_launch<false>(g, dev_err, sm_count(), st);
 }
 
 }  // namespace tpk

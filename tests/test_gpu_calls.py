@@ -25,6 +25,11 @@ SHAPES = [
     (4096, 32, 11008, 2, 1),
     (4096, 32, 11008, 8, 8),
     (512, 8, 1536, 4, 5),
+    # one-SM tiles (M <= 128) and the edge of the 256-row SM-pair tiles
+    (512, 8, 1536, 2, 128),
+    (1024, 8, 2816, 4, 100),
+    (1024, 8, 2816, 2, 129),
+    (512, 8, 1536, 4, 1000),
 ]
 
 
