@@ -291,19 +291,20 @@ def run_ours(args):
     u = torch.empty(wl.tp, M, plan.f_l, dtype=torch.bfloat16, device=dev)
     y = torch.empty(M, d, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    gscr = torch.empty(max(plan.linear_scratch_bytes(M), 16), dtype=torch.uint8, device=dev)  # stream-K partials
     stages = ["column_qkv", "attention", "row_o_reduce", "column_ffn_up_swiglu", "row_ffn_down_reduce"]
 
     def step(ev):
         ev[0].record(stream)
-        plan.column_linear(tpb.TP_QKV, x, M, blk.packed, qkv, stream)
+        plan.column_linear(tpb.TP_QKV, x, M, blk.packed, qkv, stream, scratch=gscr)
         ev[1].record(stream)
         plan.attention_heads(qkv, B, T, wl.causal, None, None, 0, 0, att, None, stream)
         ev[2].record(stream)
-        plan.row_linear_reduce(tpb.TP_ATTN_OUT, att, M, blk.packed, x, hf, ha, stream)
+        plan.row_linear_reduce(tpb.TP_ATTN_OUT, att, M, blk.packed, x, hf, ha, stream, scratch=gscr)
         ev[3].record(stream)
-        plan.column_linear(tpb.TP_FFN_UP, ha, M, blk.packed, u, stream)
+        plan.column_linear(tpb.TP_FFN_UP, ha, M, blk.packed, u, stream, scratch=gscr)
         ev[4].record(stream)
-        plan.row_linear_reduce(tpb.TP_FFN_DOWN, u, M, blk.packed, hf, y, None, stream)
+        plan.row_linear_reduce(tpb.TP_FFN_DOWN, u, M, blk.packed, hf, y, None, stream, scratch=gscr)
         ev[5].record(stream)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps + args.warmup)]

@@ -113,6 +113,10 @@ tp_status tp_plan_sizes(tp_plan_t plan, int batch, int seq,
 tp_status tp_attention_scratch_bytes(tp_plan_t plan, int batch, int seq_q, int cache_cap,
                                      size_t* bytes);
 
+/* Bytes of the optional scratch that tp_column_linear / tp_row_linear_reduce
+ * take for M token rows (0 when no kernel for that shape uses it). */
+tp_status tp_linear_scratch_bytes(tp_plan_t plan, int M, size_t* bytes);
+
 /*
  * Pack full weights (device, plan dtype, [out, in] row-major) into the
  * shard-major layout the kernels read (device, `packed`, at least
@@ -137,10 +141,17 @@ tp_status tp_shard_weights(tp_plan_t plan, const void* Wq, const void* Wk, const
  *                 each head's d_head columns contiguous, heads in order;
  *      TP_FFN_UP: n_s = d_ffn/tp, the activated U_s = silu(x Wg_s^T) *
  *                 (x Wu_s^T) (SwiGLU) or gelu(x W1_s^T) (GELU, erf form).
+ *   scratch    device, nullable, scratch_bytes >= tp_linear_scratch_bytes(M)
+ *              to be used.  With it, a GEMM whose output tiles would leave
+ *              SMs idle in the last wave splits the reduction evenly over
+ *              all SMs (stream-K: fp32 partial sums of split tiles pass
+ *              through the scratch).  Contents on entry are ignored; calls
+ *              in flight at the same time need separate scratch.
  * M >= 1.
  */
 tp_status tp_column_linear(tp_plan_t plan, int which, const void* x, int M,
-                           const void* packed, void* out_shards, void* stream);
+                           const void* packed, void* out_shards, void* scratch,
+                           size_t scratch_bytes, void* stream);
 
 /*
  * Row-parallel linear with the all-reduce fused in (same page and section:
@@ -156,10 +167,14 @@ tp_status tp_column_linear(tp_plan_t plan, int which, const void* x, int M,
  *   out_f32    device fp32 [M, d]
  *   out_act    device act [M, d], nullable: a copy of out_f32 in the plan
  *              dtype (the operand of the next column-parallel linear)
+ *   scratch    as in tp_column_linear.  With stream-K, the k-blocks of one
+ *              output tile (all shards' partials) are split between SMs and
+ *              their fp32 sums added in a fixed order by the tile's owner.
  */
 tp_status tp_row_linear_reduce(tp_plan_t plan, int which, const void* in_shards, int M,
                                const void* packed, const void* residual, void* out_f32,
-                               void* out_act, void* stream);
+                               void* out_act, void* scratch, size_t scratch_bytes,
+                               void* stream);
 
 /*
  * Per-shard multi-head attention over each shard's own heads

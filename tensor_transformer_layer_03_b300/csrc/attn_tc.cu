@@ -284,6 +284,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                // raw scores; the scale is folded into the exponent below:
+                // p = 2^(s * scale * log2(e) - m), m kept in scaled units
                 float sv[AT_KEYS];
                 {
                     uint32_t r[4][32];
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(r[c][i]) * p.scale_log2;
+                        for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(r[c][i]);
                 }
                 const int k0 = j * AT_KEYS;
                 const bool masked = (k0 + AT_KEYS > p.nkeys) || (p.causal && k0 + AT_KEYS - 1 > warp_qmin);
@@ -303,9 +305,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     for (int i = 0; i < AT_KEYS; ++i)
                         if (k0 + i > lim) sv[i] = -INFINITY;
                 }
-                float mx = sv[0];
+                // row max over 8 independent chains, then a short tree
+                float m8[8];
 #pragma unroll
-                for (int i = 1; i < AT_KEYS; ++i) mx = fmaxf(mx, sv[i]);
+                for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+#pragma unroll
+                for (int i = 8; i < AT_KEYS; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
+                                 p.scale_log2;
                 // keep the stale max unless the row max grew by more than 2^8
                 const bool grow = j == 0 || mx > m_used + RESCALE_LOG2;
                 const float m_new = grow ? fmaxf(m_used, mx) : m_used;
@@ -323,15 +331,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     tmem_st_wait();
                 }
                 m_used = m_new;
-                const float mb = m_used == -INFINITY ? 0.f : m_used;
-                float rs = 0.f;
+                const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+                float rs8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
                 for (int c = 0; c < AT_KEYS / 8; ++c) {
                     float e[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        e[i] = ex2(sv[8 * c + i] - mb);
-                        rs += e[i];
+                        e[i] = ex2(fmaf(sv[8 * c + i], p.scale_log2, neg_m));
+                        rs8[i] += e[i];
                     }
                     const uint4 v = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
                                                pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
@@ -341,6 +351,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                                  "r"(v.z), "r"(v.w)
                                  : "memory");
                 }
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 l += rs;
                 fence_async_smem();
                 tc_fence_before();

@@ -41,6 +41,10 @@ namespace tpk {
 
 namespace {
 
+#ifndef TP_GEMM_PAIR_STAGES
+#define TP_GEMM_PAIR_STAGES 6  // shared-memory ring depth of the paired kernel
+#endif
+
 constexpr int BN = 256, BK = 64;          // output columns per tile, K per stage
 constexpr int A_ROWS = 128;                // A rows staged per CTA
 constexpr int TMEM_COLS = 512;
@@ -53,7 +57,7 @@ struct GCfg {
     static constexpr int W_ROWS = PAIR ? BN / 2 : BN;  // W rows staged per CTA
     static constexpr int A_BYTES = A_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + W_ROWS * BK * 2;
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = PAIR ? TP_GEMM_PAIR_STAGES : 4;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
     // instruction descriptor: D fp32, A/B bf16, both K-major
     static constexpr uint32_t IDESC = ptx::idesc_bf16(TILE_M, BN, false);
@@ -71,9 +75,43 @@ struct Params {
     int granule;
     int* err;
     unsigned long long timeout_ns;
+    // split-K: the k-blocks of every tile are cut into `splits` equal ranges
+    // computed by different units; each writes its fp32 partial sums to
+    // partials[split][shard][row][col] (row < M, col < N) and
+    // splitk_reduce_k sums them in split order and applies the epilogue
+    int splits;
+    float* partials;
 };
 
 using namespace ptx;
+
+// One unit's work: items w = unit, unit + n_units, ... of the sequence
+// (split-major, tile-minor, so units in flight together share k ranges and
+// operand tiles); item w is tile w % n_tiles over the k-blocks of split
+// w / n_tiles.
+struct Seg {
+    int tile, split, k0, k1;
+};
+struct Sched {
+    int w, n_items, n_tiles, kbt, splits, n_units;
+    __device__ void init(const Params& p, int unit, int n_units_, int kbt_) {
+        w = unit;
+        n_units = n_units_;
+        n_tiles = p.n_tiles;
+        kbt = kbt_;
+        splits = p.splits;
+        n_items = n_tiles * splits;
+    }
+    __device__ bool next(Seg& g) {
+        if (w >= n_items) return false;
+        g.tile = w % n_tiles;
+        g.split = w / n_tiles;
+        g.k0 = (int)((long long)kbt * g.split / splits);
+        g.k1 = (int)((long long)kbt * (g.split + 1) / splits);
+        w += n_units;
+        return true;
+    }
+};
 
 __device__ __forceinline__ uint64_t sw128_kmajor(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
 
@@ -86,7 +124,9 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32], 
             d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                                pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     } else {
-        for (int i = 0; i < n_valid; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < n_valid) dst[i] = __float2bfloat16_rn(v[i]);
     }
 }
 
@@ -142,14 +182,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = unit; t < p.n_tiles && ok; t += n_units) {
+            Sched sc;
+            sc.init(p, unit, n_units, kb_per_tile);
+            Seg g;
+            while (ok && sc.next(g)) {
+                const int t = g.tile;
                 const int m_blk = t % p.m_blocks;
                 const int rest = t / p.m_blocks;
                 const int shard = p.reduce ? 0 : rest / p.n_blocks;
                 const int n_blk = p.reduce ? rest : rest % p.n_blocks;
                 const int a_row = m_blk * C::TILE_M + (int)rank * A_ROWS;
                 const int w_row = n_blk * BN + (int)rank * C::W_ROWS;
-                for (int kb = 0; kb < kb_per_tile; ++kb) {
+                for (int kb = g.k0; kb < g.k1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -186,7 +230,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int i = 0;
             bool ok = true;
-            for (int t = unit; t < p.n_tiles && ok; t += n_units, ++i) {
+            Sched sc;
+            sc.init(p, unit, n_units, kb_per_tile);
+            Seg g;
+            for (; ok && sc.next(g); ++i) {
                 const int buf = i & 1;
                 const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
                 if (!mbar_wait(&tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
@@ -195,7 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                for (int kb = 0; kb < kb_per_tile; ++kb) {
+                for (int kb = g.k0; kb < g.k1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -206,7 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t bdesc = sw128_kmajor(sa + C::A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {  // +32 bytes per K step inside the swizzle row
-                        const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                        const uint32_t acc = (kb > g.k0 || k > 0) ? 1u : 0u;
                         if constexpr (PAIR)
                             umma_f16_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), C::IDESC, acc);
                         else
@@ -246,7 +293,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // epilogue warps 2..5 -> TMEM lane quarters 2,3,0,1
         const int quarter = warp & 3;
         int i = 0;
-        for (int t = unit; t < p.n_tiles; t += n_units, ++i) {
+        Sched sc;
+        sc.init(p, unit, n_units, kb_per_tile);
+        Seg sg;
+        for (; sc.next(sg); ++i) {
+            const int t = sg.tile;
             const int buf = i & 1;
             const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
             if (!mbar_wait_warp(&tmem_full[buf], acc_phase, abort_flag, p.err, p.timeout_ns)) break;
@@ -259,7 +310,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
             const int col_base = n_blk * BN;
             const bool row_ok = row < p.M;
-            if (p.epi == EPI_SWIGLU) {
+            if (p.splits > 1) {
+                // split-K: raw fp32 partial sums of this split
+                // [split][shard][row][col]; a row-parallel launch has one output "shard"
+                const int n_sh = p.reduce ? 1 : p.shards;
+                float* dst = p.partials + (((long long)sg.split * n_sh + shard) * p.M + row) * p.N;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    __syncwarp();
+                    tmem_ld32(tbase + 32 * c, v);
+                    const int col = col_base + 32 * c;
+                    if (!row_ok || col >= p.N) continue;
+                    if (col + 32 <= p.N) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + col);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            __stcg(d4 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col + j < p.N) dst[col + j] = v[j];
+                    }
+                }
+            } else if (p.epi == EPI_SWIGLU) {
                 bf16* out = (bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo;
 #pragma unroll 1
                 for (int g = 0; g < BN / 64; ++g) {
@@ -297,7 +371,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     v[4 * q + 3] += x.w;
                                 }
                             } else {
-                                for (int j = 0; j < nv; ++j) v[j] += r[j];
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < nv) v[j] += r[j];
                             }
                         } else {
                             const bf16* r = (const bf16*)p.residual + roff + col;
@@ -314,7 +390,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     }
                                 }
                             } else {
-                                for (int j = 0; j < nv; ++j) v[j] += __bfloat162float(r[j]);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < nv) v[j] += __bfloat162float(r[j]);
                             }
                         }
                     }
@@ -324,7 +402,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int q = 0; q < 8; ++q)
                             reinterpret_cast<float4*>(o)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     } else {
-                        for (int j = 0; j < nv; ++j) o[j] = v[j];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nv) o[j] = v[j];
                     }
                     if (p.out2) store_row_bf16((bf16*)p.out2 + roff + col, v, nv);
                 }
@@ -364,6 +444,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else
             tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// Split-K second pass: out = epilogue(sum over splits of the partial sums),
+// the splits added in order 0..S-1 (the result does not depend on which SM
+// computed which split).  Four consecutive output columns per thread.
+__global__ void __launch_bounds__(256) splitk_reduce_k(Params p) {
+    const int n_out = p.epi == EPI_SWIGLU ? p.N / 2 : p.N;  // output columns per shard
+    const int n_sh = p.reduce ? 1 : p.shards;
+    const long long quads = (long long)n_sh * p.M * n_out / 4;
+    const long long split_stride = (long long)n_sh * p.M * p.N;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < quads;
+         q += (long long)gridDim.x * blockDim.x) {
+        const long long e = q * 4;
+        const int col = (int)(e % n_out);
+        const long long rs = e / n_out;  // shard * M + row
+        const int row = (int)(rs % p.M), shard = (int)(rs / p.M);
+        const float* base = p.partials + rs * p.N;
+        float v[4];
+        if (p.epi == EPI_SWIGLU) {
+            // packed columns: gate block of 32, then the matching up block
+            const int g = (col / 32) * 64 + col % 32;
+            float4 ga = __ldcg(reinterpret_cast<const float4*>(base + g));
+            float4 ua = __ldcg(reinterpret_cast<const float4*>(base + g + 32));
+            for (int sp = 1; sp < p.splits; ++sp) {
+                const float4 gb = __ldcg(reinterpret_cast<const float4*>(base + sp * split_stride + g));
+                const float4 ub = __ldcg(reinterpret_cast<const float4*>(base + sp * split_stride + g + 32));
+                ga.x += gb.x; ga.y += gb.y; ga.z += gb.z; ga.w += gb.w;
+                ua.x += ub.x; ua.y += ub.y; ua.z += ub.z; ua.w += ub.w;
+            }
+            v[0] = silu(ga.x) * ua.x;
+            v[1] = silu(ga.y) * ua.y;
+            v[2] = silu(ga.z) * ua.z;
+            v[3] = silu(ga.w) * ua.w;
+        } else {
+            float4 a = __ldcg(reinterpret_cast<const float4*>(base + col));
+            for (int sp = 1; sp < p.splits; ++sp) {
+                const float4 b = __ldcg(reinterpret_cast<const float4*>(base + sp * split_stride + col));
+                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+            }
+            v[0] = a.x;
+            v[1] = a.y;
+            v[2] = a.z;
+            v[3] = a.w;
+            if (p.epi == EPI_GELU) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = gelu_erf(v[j]);
+            }
+        }
+        if (p.epi == EPI_ROW_REDUCE) {
+            const long long o = (long long)row * p.ldo + col;
+            if (p.residual) {
+                if (p.residual_f32) {
+                    const float4 r = *reinterpret_cast<const float4*>((const float*)p.residual + o);
+                    v[0] += r.x; v[1] += r.y; v[2] += r.z; v[3] += r.w;
+                } else {
+                    const uint2 r = *reinterpret_cast<const uint2*>((const bf16*)p.residual + o);
+                    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+                    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+                    v[0] += r0.x; v[1] += r0.y; v[2] += r1.x; v[3] += r1.y;
+                }
+            }
+            *reinterpret_cast<float4*>((float*)p.out + o) = make_float4(v[0], v[1], v[2], v[3]);
+            if (p.out2)
+                *reinterpret_cast<uint2*>((bf16*)p.out2 + o) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        } else {
+            bf16* o = (bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo + col;
+            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        }
     }
 }
 
@@ -461,8 +610,12 @@ cudaError_t set_smem_attr() {
     return cudaSuccess;
 }
 
+// Largest split factor; a split keeps at least this many k-blocks.
+constexpr int SPLITK_MAX = 16, SPLITK_MIN_KB = 4;
+
 template <bool PAIR>
-cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, cudaStream_t st) {
+cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch, size_t scratch_bytes,
+                        cudaStream_t st) {
     using C = GCfg<PAIR>;
     CUtensorMap tmA, tmW;
     const uint64_t a_shards = g.reduce ? (uint64_t)g.shards : 1;
@@ -492,7 +645,22 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, cudaStream_t s
     p.granule = g.granule;
     p.err = dev_err;
     p.timeout_ns = DEFAULT_TIMEOUT_NS;
-    const int units = p.n_tiles < slots ? p.n_tiles : slots;
+    p.splits = 1;
+    // split-K when whole tiles would leave at least half of the units idle
+    if (scratch && 2 * p.n_tiles <= slots) {
+        const int kbt = (g.reduce ? g.shards : 1) * p.k_blocks;
+        int S = slots / p.n_tiles;
+        if (S > SPLITK_MAX) S = SPLITK_MAX;
+        if (S > kbt / SPLITK_MIN_KB) S = kbt / SPLITK_MIN_KB;
+        const size_t need = (size_t)S * (g.reduce ? 1 : g.shards) * g.M * g.N * sizeof(float);
+        if (S >= 2 && need <= scratch_bytes) {
+            p.splits = S;
+            p.partials = static_cast<float*>(scratch);
+        }
+    }
+    const int items = p.n_tiles * p.splits;
+    const int units = items < slots ? items : slots;
+    cudaError_t e = cudaSuccess;
     if constexpr (PAIR) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -506,16 +674,27 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, cudaStream_t s
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, tmA, tmW, p);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, tmA, tmW, p);
     } else {
         tc_gemm_kernel<false><<<units, NUM_THREADS, C::SMEM, st>>>(tmA, tmW, p);
-        return cudaGetLastError();
+        e = cudaGetLastError();
     }
+    if (e != cudaSuccess || p.splits == 1) return e;
+    const long long quads = (long long)(g.reduce ? 1 : g.shards) * g.M * (g.epi == EPI_SWIGLU ? g.N / 2 : g.N) / 4;
+    long long blocks = (quads + 255) / 256;
+    if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
+    splitk_reduce_k<<<(unsigned)blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st) {
+size_t tc_gemm_scratch_bytes() {
+    // S * tiles <= units, so the partials never exceed one 128 x 256 fp32 tile per SM
+    return (size_t)sm_count() * A_ROWS * BN * sizeof(float);
+}
+
+cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st) {
     if (g.epi == EPI_SWIGLU && (g.granule != 32 || g.N % 64 != 0)) return cudaErrorNotSupported;
     cudaError_t e = set_smem_attr<false>();
     if (e == cudaSuccess) e = set_smem_attr<true>();
@@ -523,9 +702,9 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st) {
     // 2-SM tiles once there is more than one 128-row block of tokens
     if (g.M > A_ROWS) {
         const int slots = pair_slots();
-        if (slots > 0) return gemm_launch<true>(g, dev_err, slots, st);
+        if (slots > 0) return gemm_launch<true>(g, dev_err, slots, scratch, scratch_bytes, st);
     }
-    return gemm_launch<false>(g, dev_err, sm_count(), st);
+    return gemm_launch<false>(g, dev_err, sm_count(), scratch, scratch_bytes, st);
 }
 
 }  // namespace tpk

@@ -76,7 +76,10 @@ struct TcGemm {
     int residual_f32;
 };
 bool tc_gemm_supported(int M, int N, int K);
-cudaError_t tc_gemm(const TcGemm& g, int* dev_err, cudaStream_t st);
+// scratch (nullable): stream-K partials and flags, at least
+// tc_gemm_scratch_bytes() to be used; without it every launch runs whole tiles
+size_t tc_gemm_scratch_bytes();
+cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st);
 
 // ---- small-M weight streaming (gemv.cu): same arguments as the GEMM ---------
 typedef TcGemm GemvArgs;

@@ -45,13 +45,10 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
-// Bounded wait (one thread) for the phase of parity `parity`.  Returns false
-// when the CTA aborted (another role timed out) or this wait timed out (then
-// it records the error and raises the abort flag).
-__device__ __noinline__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                              unsigned long long timeout_ns) {
+// Slow path of mbar_wait: poll with a deadline.
+__device__ __noinline__ inline bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* err, unsigned long long timeout_ns) {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
@@ -64,6 +61,17 @@ __device__ __noinline__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, vo
             }
         }
     }
+}
+
+// Bounded wait (one thread) for the phase of parity `parity`.  Returns false
+// when the CTA aborted (another role timed out) or this wait timed out (then
+// it records the error and raises the abort flag).  The common case (phase
+// already complete, or completing within the hardware's try_wait window) is
+// inline; only a real wait calls the polling loop.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          unsigned long long timeout_ns) {
+    if (mbar_try_wait(smem_u32(bar), parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, err, timeout_ns);
 }
 
 // The same wait taken by a whole warp: every lane polls, the warp leaves

@@ -40,8 +40,15 @@ int* device_error_word() {
 }
 
 struct Workspace {
-    size_t qkv, attn, hf32, hact, u, scratch, total;
+    size_t qkv, attn, hf32, hact, u, scratch, gemm, total;
 };
+
+// Stream-K scratch of the tensor-core GEMMs (bf16 plans, M past the
+// weight-streaming range); 0 when no GEMM of this shape would use it.
+size_t linear_scratch_bytes(const tp_plan_s* p, long long M) {
+    if (p->dtype != TP_BF16 || M <= tpk::GEMV_MAX_M) return 0;
+    return tpk::tc_gemm_scratch_bytes();
+}
 
 size_t attn_scratch_bytes(const tp_plan_s* p, int batch, int seq_q) {
     if (seq_q != 1) return 0;
@@ -58,6 +65,7 @@ Workspace workspace_layout(const tp_plan_s* p, int batch, int seq) {
     w.hact = o;  o = align_up(o + M * p->d * es, 1024);
     w.u = o;     o = align_up(o + (size_t)p->tp * M * p->fl * es, 1024);
     w.scratch = o; o = align_up(o + attn_scratch_bytes(p, batch, seq), 1024);
+    w.gemm = o;    o = align_up(o + linear_scratch_bytes(p, (long long)batch * seq), 1024);
     w.total = o;
     return w;
 }
@@ -156,6 +164,13 @@ tp_status tp_attention_scratch_bytes(tp_plan_t p, int batch, int seq_q, int cach
     return TP_OK;
 }
 
+tp_status tp_linear_scratch_bytes(tp_plan_t p, int M, size_t* bytes) {
+    if (!p || !bytes) return TP_ERR_NULL_ARG;
+    if (M <= 0) return TP_ERR_INVALID_DIM;
+    *bytes = linear_scratch_bytes(p, M);
+    return TP_OK;
+}
+
 tp_status tp_shard_weights(tp_plan_t p, const void* Wq, const void* Wk, const void* Wv, const void* Wo,
                            const void* W1_or_Wgate, const void* Wup, const void* Wdown, void* packed,
                            void* stream) {
@@ -175,10 +190,11 @@ tp_status tp_shard_weights(tp_plan_t p, const void* Wq, const void* Wk, const vo
 }
 
 tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const void* packed, void* out_shards,
-                           void* stream) {
+                           void* scratch, size_t scratch_bytes, void* stream) {
     if (!p || !x || !packed || !out_shards) return TP_ERR_NULL_ARG;
     if (M <= 0 || (which != TP_QKV && which != TP_FFN_UP)) return TP_ERR_INVALID_DIM;
-    if (misaligned(x) || misaligned(packed) || misaligned(out_shards)) return TP_ERR_ALIGNMENT;
+    if (misaligned(x) || misaligned(packed) || misaligned(out_shards) || misaligned(scratch))
+        return TP_ERR_ALIGNMENT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool qkv = which == TP_QKV;
     const int N = qkv ? 3 * p->hl * p->dh : p->up_rows;  // W rows per shard
@@ -204,7 +220,7 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
         g.granule = p->granule;
         if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, st));
         if (tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32))
-            return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
+            return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
     tpk::SimtGemm g{};
     g.epi = epi;
@@ -228,11 +244,12 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
 }
 
 tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
-                               const void* residual, void* out_f32, void* out_act, void* stream) {
+                               const void* residual, void* out_f32, void* out_act, void* scratch,
+                               size_t scratch_bytes, void* stream) {
     if (!p || !in_shards || !packed || !out_f32) return TP_ERR_NULL_ARG;
     if (M <= 0 || (which != TP_ATTN_OUT && which != TP_FFN_DOWN)) return TP_ERR_INVALID_DIM;
     if (misaligned(in_shards) || misaligned(packed) || misaligned(residual) || misaligned(out_f32) ||
-        misaligned(out_act))
+        misaligned(out_act) || misaligned(scratch))
         return TP_ERR_ALIGNMENT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool attn = which == TP_ATTN_OUT;
@@ -258,7 +275,8 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
         g.residual = residual;
         g.residual_f32 = res_f32;
         if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, st));
-        if (tpk::tc_gemm_supported(M, p->d, ks)) return cuda_status(tpk::tc_gemm(g, device_error_word(), st));
+        if (tpk::tc_gemm_supported(M, p->d, ks))
+            return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
     tpk::SimtGemm g{};
     g.epi = tpk::EPI_ROW_REDUCE;
@@ -344,16 +362,18 @@ tp_status tp_block_forward(tp_plan_t p, const void* x, int batch, int seq, int c
     void* hf32 = ptr_at(workspace, w.hf32);
     void* hact = ptr_at(workspace, w.hact);
     void* u = ptr_at(workspace, w.u);
-    tp_status s = tp_column_linear(p, TP_QKV, x, M, packed, qkv, stream);
+    void* gs = w.total > w.gemm ? ptr_at(workspace, w.gemm) : nullptr;
+    const size_t gsb = w.total - w.gemm;
+    tp_status s = tp_column_linear(p, TP_QKV, x, M, packed, qkv, gs, gsb, stream);
     if (s != TP_OK) return s;
     s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
-                           ptr_at(workspace, w.scratch), w.total - w.scratch, stream);
+                           ptr_at(workspace, w.scratch), w.gemm - w.scratch, stream);
     if (s != TP_OK) return s;
-    s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, stream);
+    s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
     if (s != TP_OK) return s;
-    s = tp_column_linear(p, TP_FFN_UP, hact, M, packed, u, stream);
+    s = tp_column_linear(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, stream);
     if (s != TP_OK) return s;
-    return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, nullptr, stream);
+    return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, nullptr, gs, gsb, stream);
 }
 
 tp_status tp_sync_status(void* stream) {

@@ -45,8 +45,9 @@ EXPORTS = {
     "tp_plan_sizes": (_i, [_p, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     "tp_attention_scratch_bytes": (_i, [_p, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tp_shard_weights": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
-    "tp_column_linear": (_i, [_p, _i, _p, _i, _p, _p, _p]),
-    "tp_row_linear_reduce": (_i, [_p, _i, _p, _i, _p, _p, _p, _p, _p]),
+    "tp_linear_scratch_bytes": (_i, [_p, _i, ctypes.POINTER(_sz)]),
+    "tp_column_linear": (_i, [_p, _i, _p, _i, _p, _p, _p, _sz, _p]),
+    "tp_row_linear_reduce": (_i, [_p, _i, _p, _i, _p, _p, _p, _p, _p, _sz, _p]),
     "tp_attention_heads": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p]),
     "tp_block_forward": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p, _p]),
     "tp_attention_decode_noalloc": (_i, [_p, _p, _i, _p, _p, _i, _i, _p, _p]),
@@ -132,13 +133,21 @@ class Plan:
                                _ptr(first), _ptr(up), _ptr(w["Wd"]), _ptr(packed), _stream(stream)),
               "tp_shard_weights")
 
-    def column_linear(self, which, x, M, packed, out, stream=None):
-        check(tp_column_linear(self.handle, which, _ptr(x), M, _ptr(packed), _ptr(out), _stream(stream)),
-              "tp_column_linear")
+    def linear_scratch_bytes(self, M):
+        b = _sz()
+        check(tp_linear_scratch_bytes(self.handle, M, ctypes.byref(b)), "tp_linear_scratch_bytes")
+        return b.value
 
-    def row_linear_reduce(self, which, inp, M, packed, residual, out_f32, out_act=None, stream=None):
+    def column_linear(self, which, x, M, packed, out, stream=None, scratch=None):
+        nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+        check(tp_column_linear(self.handle, which, _ptr(x), M, _ptr(packed), _ptr(out), _ptr(scratch), nbytes,
+                               _stream(stream)), "tp_column_linear")
+
+    def row_linear_reduce(self, which, inp, M, packed, residual, out_f32, out_act=None, stream=None, scratch=None):
+        nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
         check(tp_row_linear_reduce(self.handle, which, _ptr(inp), M, _ptr(packed), _ptr(residual),
-                                   _ptr(out_f32), _ptr(out_act), _stream(stream)), "tp_row_linear_reduce")
+                                   _ptr(out_f32), _ptr(out_act), _ptr(scratch), nbytes, _stream(stream)),
+              "tp_row_linear_reduce")
 
     def attention_heads(self, qkv, batch, seq_q, causal, k_cache, v_cache, cache_cap, cache_pos, out,
                         scratch=None, stream=None):

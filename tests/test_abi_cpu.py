@@ -114,15 +114,25 @@ def test_argument_validation_before_launch(tp):
     P = lambda v: ctypes.c_void_p(v)  # fake device addresses: never dereferenced
     good, odd = P(0x10000), P(0x10008)
     # column linear
-    assert tp.tp_column_linear(None, 0, good, 4, good, good, None) == 1
-    assert tp.tp_column_linear(h, 0, None, 4, good, good, None) == 1
-    assert tp.tp_column_linear(h, 0, good, 0, good, good, None) == 2
-    assert tp.tp_column_linear(h, 5, good, 4, good, good, None) == 2
-    assert tp.tp_column_linear(h, 0, odd, 4, good, good, None) == 7
+    CL = tp.tp_column_linear
+    assert CL(None, 0, good, 4, good, good, None, 0, None) == 1
+    assert CL(h, 0, None, 4, good, good, None, 0, None) == 1
+    assert CL(h, 0, good, 0, good, good, None, 0, None) == 2
+    assert CL(h, 5, good, 4, good, good, None, 0, None) == 2
+    assert CL(h, 0, odd, 4, good, good, None, 0, None) == 7
+    assert CL(h, 0, good, 4, good, good, odd, 1 << 20, None) == 7   # misaligned scratch
     # row reduce
-    assert tp.tp_row_linear_reduce(h, 0, good, 4, good, None, None, None, None) == 1
-    assert tp.tp_row_linear_reduce(h, 3, good, 4, good, None, good, None, None) == 2
-    assert tp.tp_row_linear_reduce(h, 1, good, 4, good, odd, good, None, None) == 7
+    RR = tp.tp_row_linear_reduce
+    assert RR(h, 0, good, 4, good, None, None, None, None, 0, None) == 1
+    assert RR(h, 3, good, 4, good, None, good, None, None, 0, None) == 2
+    assert RR(h, 1, good, 4, good, odd, good, None, None, 0, None) == 7
+    assert RR(h, 1, good, 4, good, None, good, None, odd, 1 << 20, None) == 7
+    # scratch size query
+    sb = ctypes.c_size_t()
+    assert tp.tp_linear_scratch_bytes(None, 4, ctypes.byref(sb)) == 1
+    assert tp.tp_linear_scratch_bytes(h, 0, ctypes.byref(sb)) == 2
+    assert tp.tp_linear_scratch_bytes(h, 4, ctypes.byref(sb)) == 0 and sb.value == 0  # weight-streaming rows
+    assert tp.tp_linear_scratch_bytes(h, 512, ctypes.byref(sb)) == 0 and sb.value > 0
     # attention
     A = tp.tp_attention_heads
     assert A(h, good, 1, 4, 1, good, None, 8, 0, good, None, 0, None) == 1      # one-sided cache

@@ -49,21 +49,28 @@ def _packed(tp_mod, plan, shape, dtype, seed):
     return w, packed
 
 
+def _scratch(plan, M, use):
+    """Stream-K scratch for the linears (None: whole-tile schedule)."""
+    n = plan.linear_scratch_bytes(M) if use else 0
+    return torch.empty(n, dtype=torch.uint8, device=DEV) if n else None
+
+
 def _check(got, ref, dtype, what):
     if dtype == "bf16":
         return assert_close_bf16(got, ref, what)
     return assert_close_fp32(got, ref, what)
 
 
+@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "splitk"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
-def test_column_qkv(tp, d, H, f, deg, M, dtype):
+def test_column_qkv(tp, d, H, f, deg, M, dtype, sk):
     plan = _plan(tp, d, H, f, deg, dtype=dtype)
     shape = I.BlockShape(d, H, f, "swiglu")
     w, packed = _packed(tp, plan, shape, dtype, 1)
     x = I.make_matrix(M, d, dtype, _gen(2))
     out = torch.empty(deg, M, 3 * d // deg, dtype=I.torch_dtype(dtype), device=DEV)
-    plan.column_linear(tp.TP_QKV, x.to(DEV), M, packed, out)
+    plan.column_linear(tp.TP_QKV, x.to(DEV), M, packed, out, scratch=_scratch(plan, M, sk))
     plan.sync_status()
     ref = qkv_shards(o.linear(x, w["Wq"]), o.linear(x, w["Wk"]), o.linear(x, w["Wv"]), deg, H)
     if dtype == "bf16":
@@ -71,16 +78,17 @@ def test_column_qkv(tp, d, H, f, deg, M, dtype):
     _check(out, ref, dtype, "QKV")
 
 
+@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "splitk"])
 @pytest.mark.parametrize("act", ["swiglu", "gelu"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
-def test_column_ffn_up(tp, d, H, f, deg, M, dtype, act):
+def test_column_ffn_up(tp, d, H, f, deg, M, dtype, act, sk):
     plan = _plan(tp, d, H, f, deg, act=act, dtype=dtype)
     shape = I.BlockShape(d, H, f, act)
     w, packed = _packed(tp, plan, shape, dtype, 3)
     h = I.make_matrix(M, d, dtype, _gen(4))
     out = torch.empty(deg, M, f // deg, dtype=I.torch_dtype(dtype), device=DEV)
-    plan.column_linear(tp.TP_FFN_UP, h.to(DEV), M, packed, out)
+    plan.column_linear(tp.TP_FFN_UP, h.to(DEV), M, packed, out, scratch=_scratch(plan, M, sk))
     plan.sync_status()
     if act == "swiglu":
         u = o.silu(o.linear(h, w["Wg"])) * o.linear(h, w["Wu"])
@@ -92,10 +100,11 @@ def test_column_ffn_up(tp, d, H, f, deg, M, dtype, act):
     _check(out, ref, dtype, f"FFN-up {act}")
 
 
+@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "splitk"])
 @pytest.mark.parametrize("which", ["attn_out", "ffn_down"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
-def test_row_reduce(tp, d, H, f, deg, M, dtype, which):
+def test_row_reduce(tp, d, H, f, deg, M, dtype, which, sk):
     plan = _plan(tp, d, H, f, deg, dtype=dtype)
     shape = I.BlockShape(d, H, f, "swiglu")
     w, packed = _packed(tp, plan, shape, dtype, 5)
@@ -112,7 +121,8 @@ def test_row_reduce(tp, d, H, f, deg, M, dtype, which):
         code = tp.TP_FFN_DOWN
     out = torch.empty(M, d, dtype=torch.float32, device=DEV)
     out_act = torch.empty(M, d, dtype=I.torch_dtype(dtype), device=DEV)
-    plan.row_linear_reduce(code, inp.to(DEV), M, packed, res.to(DEV), out, out_act)
+    scr = _scratch(plan, M, sk)
+    plan.row_linear_reduce(code, inp.to(DEV), M, packed, res.to(DEV), out, out_act, scratch=scr)
     plan.sync_status()
     a_full = unshard_cols(inp)
     ref = np64(res) + o.all_reduce_sum(o.row_parallel_partials(a_full, W, deg))
@@ -124,7 +134,7 @@ def test_row_reduce(tp, d, H, f, deg, M, dtype, which):
     assert nw <= fp32_bound, nw
     _check(out_act, o.round_bf16(ref) if dtype == "bf16" else ref, dtype, "row act copy")
     # without residual and without the act copy
-    plan.row_linear_reduce(code, inp.to(DEV), M, packed, None, out, None)
+    plan.row_linear_reduce(code, inp.to(DEV), M, packed, None, out, None, scratch=scr)
     plan.sync_status()
     ref0 = ref - np64(res)
     assert float(np.max(np.abs(np64(out) - ref0)) / np.max(np.abs(ref0))) <= fp32_bound
