@@ -233,18 +233,202 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_split_bf16_k(AttnArgs a, f
     }
 }
 
+// bf16 single-token pass 1, latency-lean: one block per (sequence, head,
+// chunk of 64 keys).  Every thread issues all of its K and V loads up front
+// (a key row is split between two threads), so a chunk costs one memory
+// round trip; the new token's K/V row (position pos) is read from the QKV
+// buffer and written into the cache by the block that owns it, so no
+// separate append pass runs.  Scores in log2 units; partial (m, l, o) as in
+// the kernels above.
+constexpr int DC_KEYS = 64;
+
+template <int DH>
+__global__ void __launch_bounds__(DEC_THREADS) decode_chunk_bf16_k(AttnArgs a, float* __restrict__ part) {
+    constexpr int CH = DH / 8;        // 16-byte chunks per key row
+    constexpr int CPT = CH / 2;       // chunks per thread (half a row)
+    constexpr int G = DEC_THREADS / DH;
+    __shared__ float qs[DH];
+    __shared__ __align__(16) bf16 vs[DC_KEYS][DH];
+    __shared__ float ps[DC_KEYS];
+    __shared__ float red[DEC_THREADS / 32];
+    __shared__ float ored[G][DH];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int s = h / a.hl, jl = h % a.hl;
+    const int t = threadIdx.x;
+    const int L = a.pos + 1;
+    const int k0 = c * DC_KEYS;
+    const int key = k0 + t / 2, half = t % 2;
+    const bool have = key < L;
+    const bf16* qkv_row = (const bf16*)a.qkv + ((long long)s * a.B + b) * (3 * a.hl * DH);
+    bf16* kcache = (bf16*)a.kc + ((long long)b * a.H + h) * a.cap * DH;
+    bf16* vcache = (bf16*)a.vc + ((long long)b * a.H + h) * a.cap * DH;
+    // everything read below (Q, the new K/V, and cache rows appended by
+    // earlier steps' kernels) may come from kernels still finishing
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    uint4 kv[CPT], vv[CPT];
+    const bool is_new = key == a.pos;
+    if (have && !is_new) {
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            kv[i] = reinterpret_cast<const uint4*>(kcache + (long long)key * DH)[half * CPT + i];
+            vv[i] = reinterpret_cast<const uint4*>(vcache + (long long)key * DH)[half * CPT + i];
+        }
+    }
+    if (is_new) {
+        const uint4* kn = reinterpret_cast<const uint4*>(qkv_row + (a.hl + jl) * DH) + half * CPT;
+        const uint4* vn = reinterpret_cast<const uint4*>(qkv_row + (2 * a.hl + jl) * DH) + half * CPT;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            kv[i] = kn[i];
+            vv[i] = vn[i];
+            reinterpret_cast<uint4*>(kcache + (long long)key * DH)[half * CPT + i] = kv[i];
+            reinterpret_cast<uint4*>(vcache + (long long)key * DH)[half * CPT + i] = vv[i];
+        }
+    }
+    const float sl2 = a.scale * 1.4426950408889634f;
+    for (int i = t; i < DH; i += DEC_THREADS) qs[i] = __bfloat162float(qkv_row[jl * DH + i]) * sl2;
+    __syncthreads();
+    // score of this thread's key: its half-row dot q, then the partner's half
+    float d = 0.f;
+    if (have) {
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&kv[i]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(hk[e]);
+                const int dim = (half * CPT + i) * 8 + 2 * e;
+                d = fmaf(qs[dim], f.x, d);
+                d = fmaf(qs[dim + 1], f.y, d);
+            }
+        }
+    }
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    const float sc = have ? d : -INFINITY;
+    if (have) {
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) reinterpret_cast<uint4*>(&vs[t / 2][0])[half * CPT + i] = vv[i];
+    }
+    const float m = block_reduce(sc, red, true);
+    const float pr = have ? exp2f(sc - m) : 0.f;
+    if (half == 0) ps[t / 2] = pr;
+    const float l = block_reduce(half == 0 ? pr : 0.f, red, false);  // its barriers publish ps[] and vs[]
+    // o[dim] = sum_k p_k v[k][dim]; G key groups per dimension
+    const int dim = t % DH, grp = t / DH;
+    const int nk = min(DC_KEYS, L - k0);
+    float o = 0.f;
+#pragma unroll 8
+    for (int k = grp; k < nk; k += G) o = fmaf(ps[k], __bfloat162float(vs[k][dim]), o);
+    ored[grp][dim] = o;
+    __syncthreads();
+    float* dst = part + (((long long)b * a.H + h) * DECODE_MAX_SPLITS + c) * (DH + 2);
+    if (t < DH) {
+        float acc = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) acc += ored[g2][t];
+        dst[2 + t] = acc;
+    }
+    if (t == 0) {
+        dst[0] = m;
+        dst[1] = l;
+    }
+}
+
+// bf16 pass 2: merge the chunks of one (sequence, head).  The chunk maxima
+// and sums are read in parallel (one chunk per thread), then each thread
+// sums one output dimension over the chunks.
+template <int DH>
+__global__ void __launch_bounds__(DH) decode_merge_bf16_k(AttnArgs a, const float* __restrict__ part, int nsplit) {
+    __shared__ float w[DECODE_MAX_SPLITS];
+    __shared__ float red[DH / 32 > 0 ? DH / 32 : 1];
+    __shared__ float tot;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int s = h / a.hl, jl = h % a.hl;
+    const int t = threadIdx.x;
+    const float* src = part + ((long long)b * a.H + h) * DECODE_MAX_SPLITS * (DH + 2);
+    float mc = -INFINITY, lc = 0.f;
+    for (int c = t; c < nsplit; c += DH) {
+        mc = fmaxf(mc, src[c * (DH + 2)]);
+    }
+    // block max of the chunk maxima
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+    if (t % 32 == 0) red[t / 32] = mc;
+    __syncthreads();
+    float mx = red[0];
+#pragma unroll
+    for (int i = 1; i < DH / 32; ++i) mx = fmaxf(mx, red[i]);
+    for (int c = t; c < nsplit; c += DH) {
+        const float wc = exp2f(src[c * (DH + 2)] - mx);
+        w[c] = wc;
+        lc = fmaf(src[c * (DH + 2) + 1], wc, lc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lc += __shfl_xor_sync(0xffffffffu, lc, off);
+    __syncthreads();
+    if (t % 32 == 0) red[t / 32] = lc;
+    __syncthreads();
+    if (t == 0) {
+        float l = 0.f;
+        for (int i = 0; i < DH / 32; ++i) l += red[i];
+        tot = l;
+    }
+    __syncthreads();
+    float o = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < nsplit; ++c) o = fmaf(src[c * (DH + 2) + 2 + t], w[c], o);
+    bf16* out = (bf16*)a.out + ((long long)s * a.B + b) * (a.hl * DH) + jl * DH;
+    out[t] = __float2bfloat16_rn(o / tot);
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel in the stream finishes; it waits
+// (griddepcontrol.wait) before reading what that kernel wrote.
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <typename T, int DH>
 cudaError_t decode_launch(const AttnArgs& a, float* scratch, cudaStream_t st) {
     const int L = a.pos + 1;
     int nsplit, chunk;
     if (a.is_bf16) {
-        // chunks of about 64 keys, at most DECODE_MAX_SPLITS of them
+        if (DH == 64 || DH == 128) {
+            nsplit = (L + DC_KEYS - 1) / DC_KEYS;
+            if (nsplit <= DECODE_MAX_SPLITS) {
+                cudaError_t e = launch_pdl(decode_chunk_bf16_k<DH>, dim3(nsplit, a.H, a.B), dim3(DEC_THREADS), st, a,
+                                           scratch);
+                if (e != cudaSuccess) return e;
+                return launch_pdl(decode_merge_bf16_k<DH>, dim3(a.H, a.B), dim3(DH), st, a,
+                                  static_cast<const float*>(scratch), nsplit);
+            }
+        }
+        // long caches (or other head widths): chunks of about 64 keys, at most
+        // DECODE_MAX_SPLITS of them, after a separate append of the new K/V
+        cudaError_t e = kv_append(a, const_cast<void*>(a.kc), const_cast<void*>(a.vc), st);
+        if (e != cudaSuccess) return e;
         nsplit = (L + 63) / 64;
         if (nsplit > DECODE_MAX_SPLITS) nsplit = DECODE_MAX_SPLITS;
         chunk = (L + nsplit - 1) / nsplit;
         nsplit = (L + chunk - 1) / chunk;
         decode_split_bf16_k<DH><<<dim3(nsplit, a.H, a.B), DEC_THREADS, 0, st>>>(a, scratch, chunk);
     } else {
+        cudaError_t e = kv_append(a, const_cast<void*>(a.kc), const_cast<void*>(a.vc), st);
+        if (e != cudaSuccess) return e;
         nsplit = (L + DEC_THREADS - 1) / DEC_THREADS;
         chunk = DEC_THREADS;
         if (nsplit > DECODE_MAX_SPLITS) {

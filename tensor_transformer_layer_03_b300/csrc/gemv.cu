@@ -25,7 +25,7 @@ namespace {
 
 constexpr int GV_THREADS = 256;
 constexpr int GV_WARPS = GV_THREADS / 32;
-constexpr int GV_UNROLL = 8;  // 16-byte weight loads in flight per lane
+constexpr int GV_UNROLL = 8;  // 16-byte weight loads in flight per lane and row
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
     uint4 v;
@@ -48,6 +48,16 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
     }
     return s;
 }
+
+// Start pulling `bytes` (a multiple of 16) at p into L2 without waiting.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// Programmatic dependent launch: let the next kernel in the stream start
+// (it waits for this one before reading its outputs) / wait for the
+// previous kernel's results.  No-ops when the launch did not allow it.
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -81,12 +91,66 @@ __device__ __forceinline__ void row_dots(const bf16* __restrict__ w, const bf16*
     }
 }
 
+// The same for two weight rows at once (w0 with inputs x0, w1 with x1):
+// their loads are issued together, 2 * GV_UNROLL in flight per lane.
+template <int MT>
+__device__ __forceinline__ void row_dots2(const bf16* __restrict__ w0, const bf16* __restrict__ x0,
+                                          const bf16* __restrict__ w1, const bf16* __restrict__ x1, long long ldx,
+                                          int K, float (&acc0)[MT], float (&acc1)[MT]) {
+    const int lane = threadIdx.x % 32;
+    const int nch = K / 8;
+    int c = lane;
+    for (; c + 32 * (GV_UNROLL - 1) < nch; c += 32 * GV_UNROLL) {
+        uint4 v0[GV_UNROLL], v1[GV_UNROLL];
+#pragma unroll
+        for (int u = 0; u < GV_UNROLL; ++u) {
+            v0[u] = ld_stream(w0 + (c + 32 * u) * 8);
+            v1[u] = ld_stream(w1 + (c + 32 * u) * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < GV_UNROLL; ++u) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                acc0[m] += dot8(v0[u], __ldg(reinterpret_cast<const uint4*>(x0 + m * ldx + (c + 32 * u) * 8)));
+                acc1[m] += dot8(v1[u], __ldg(reinterpret_cast<const uint4*>(x1 + m * ldx + (c + 32 * u) * 8)));
+            }
+        }
+    }
+    for (; c < nch; c += 32) {
+        const uint4 a = ld_stream(w0 + c * 8), b = ld_stream(w1 + c * 8);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            acc0[m] += dot8(a, __ldg(reinterpret_cast<const uint4*>(x0 + m * ldx + c * 8)));
+            acc1[m] += dot8(b, __ldg(reinterpret_cast<const uint4*>(x1 + m * ldx + c * 8)));
+        }
+    }
+}
+
 template <int MT, int EPI>
 __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gw = blockIdx.x * GV_WARPS + warp, nw = gridDim.x * GV_WARPS;
     const bf16* W = (const bf16*)g.W;
     const bf16* X = (const bf16*)g.A;
+    pdl_launch_next();
+    // the packed weights are written only by the packing kernels, never by a
+    // kernel this one can overlap: start this warp's first rows toward L2
+    // before waiting for the input rows
+    if (lane == 0) {
+        const uint32_t row_bytes = (uint32_t)g.K * 2;
+        if (EPI == EPI_SWIGLU) {
+            const int n_out = g.N / 2;
+            if (gw < g.shards * n_out) {
+                const int s = gw / n_out, j = gw % n_out;
+                const long long gate_row = (long long)s * g.N + (j / g.granule) * 2 * g.granule + j % g.granule;
+                prefetch_l2(W + gate_row * g.K, row_bytes);
+                prefetch_l2(W + (gate_row + g.granule) * g.K, row_bytes);
+            }
+        } else if (gw < g.shards * g.N) {
+            prefetch_l2(W + (long long)gw * g.K, row_bytes);
+        }
+    }
+    pdl_wait_prev();
     if (EPI == EPI_SWIGLU) {
         const int n_out = g.N / 2;  // U columns per shard
         const int items = g.shards * n_out;
@@ -97,8 +161,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
             float ag[MT], au[MT];
 #pragma unroll
             for (int m = 0; m < MT; ++m) ag[m] = au[m] = 0.f;
-            row_dots<MT>(W + gate_row * g.K, X, g.lda, g.K, ag);
-            row_dots<MT>(W + (gate_row + g.granule) * g.K, X, g.lda, g.K, au);
+            row_dots2<MT>(W + gate_row * g.K, X, W + (gate_row + g.granule) * g.K, X, g.lda, g.K, ag, au);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const float gs = warp_sum(ag[m]), us = warp_sum(au[m]);
@@ -107,18 +170,28 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
             }
         }
     } else {
+        // items it and it + nw together (two rows' loads in flight)
         const int items = g.shards * g.N;
-        for (int it = gw; it < items; it += nw) {
-            const int s = it / g.N, n = it % g.N;
-            float acc[MT];
+        for (int it = gw; it < items; it += 2 * nw) {
+            const int it2 = it + nw;
+            float acc[2][MT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-            row_dots<MT>(W + (long long)it * g.K, X, g.lda, g.K, acc);
+            for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
+            if (it2 < items)
+                row_dots2<MT>(W + (long long)it * g.K, X, W + (long long)it2 * g.K, X, g.lda, g.K, acc[0], acc[1]);
+            else
+                row_dots<MT>(W + (long long)it * g.K, X, g.lda, g.K, acc[0]);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float v = warp_sum(acc[m]);
-                if (EPI == EPI_GELU) v = gelu_erf(v);
-                if (lane == 0) ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + n] = __float2bfloat16_rn(v);
+            for (int r = 0; r < 2; ++r) {
+                const int itr = r ? it2 : it;
+                if (itr >= items) break;
+                const int s = itr / g.N, n = itr % g.N;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float v = warp_sum(acc[r][m]);
+                    if (EPI == EPI_GELU) v = gelu_erf(v);
+                    if (lane == 0) ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + n] = __float2bfloat16_rn(v);
+                }
             }
         }
     }
@@ -131,12 +204,26 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_row_k(GemvArgs g) {
     const int gw = blockIdx.x * GV_WARPS + warp, nw = gridDim.x * GV_WARPS;
     const bf16* W = (const bf16*)g.W;
     const bf16* A = (const bf16*)g.A;
+    pdl_launch_next();
+    if (lane == 0 && gw < g.N)  // first output row's weights, every shard (see gemv_col_k)
+        for (int s = 0; s < g.shards; ++s) prefetch_l2(W + s * g.w_shard + (long long)gw * g.K, (uint32_t)g.K * 2);
+    pdl_wait_prev();
     for (int n = gw; n < g.N; n += nw) {
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-        for (int s = 0; s < g.shards; ++s)  // shard order: the fused all-reduce
-            row_dots<MT>(W + s * g.w_shard + (long long)n * g.K, A + s * g.a_shard, g.lda, g.K, acc);
+        // shards in order (the fused all-reduce), two rows' loads in flight
+        int s = 0;
+        for (; s + 1 < g.shards; s += 2) {
+            float a1[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) a1[m] = 0.f;
+            row_dots2<MT>(W + s * g.w_shard + (long long)n * g.K, A + s * g.a_shard,
+                          W + (s + 1) * g.w_shard + (long long)n * g.K, A + (s + 1) * g.a_shard, g.lda, g.K, acc, a1);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] += a1[m];
+        }
+        if (s < g.shards) row_dots<MT>(W + s * g.w_shard + (long long)n * g.K, A + s * g.a_shard, g.lda, g.K, acc);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             float v = warp_sum(acc[m]);
@@ -160,21 +247,35 @@ int sm_count_dev() {
     return n[dev] > 0 ? n[dev] : 148;
 }
 
+// Grid: every warp gets the same number of items (ceil(items / warps)),
+// with all blocks resident at once, so no partial second wave trails.
+// Launched with programmatic dependent launch allowed.
 template <int MT>
 cudaError_t gemv_launch(const GemvArgs& g, cudaStream_t st) {
     const int items = g.reduce ? g.N : g.shards * (g.epi == EPI_SWIGLU ? g.N / 2 : g.N);
-    int blocks = (items + GV_WARPS - 1) / GV_WARPS;
-    const int cap = sm_count_dev() * 16;
-    if (blocks > cap) blocks = cap;
-    if (g.reduce)
-        gemv_row_k<MT><<<blocks, GV_THREADS, 0, st>>>(g);
-    else if (g.epi == EPI_SWIGLU)
-        gemv_col_k<MT, EPI_SWIGLU><<<blocks, GV_THREADS, 0, st>>>(g);
-    else if (g.epi == EPI_GELU)
-        gemv_col_k<MT, EPI_GELU><<<blocks, GV_THREADS, 0, st>>>(g);
-    else
-        gemv_col_k<MT, EPI_STORE><<<blocks, GV_THREADS, 0, st>>>(g);
-    return cudaGetLastError();
+    void (*kern)(GemvArgs) = g.reduce ? gemv_row_k<MT>
+                             : g.epi == EPI_SWIGLU ? gemv_col_k<MT, EPI_SWIGLU>
+                             : g.epi == EPI_GELU   ? gemv_col_k<MT, EPI_GELU>
+                                                   : gemv_col_k<MT, EPI_STORE>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, GV_THREADS, 0) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    const int resident_warps = sm_count_dev() * per_sm * GV_WARPS;
+    const int per_warp = (items + resident_warps - 1) / resident_warps;
+    const int warps = (items + per_warp - 1) / per_warp;
+    const int blocks = (warps + GV_WARPS - 1) / GV_WARPS;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(blocks > 0 ? blocks : 1);
+    cfg.blockDim = dim3(GV_THREADS);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, g);
 }
 
 }  // namespace
@@ -184,7 +285,7 @@ bool gemv_supported(const GemvArgs& g) {
            (g.epi != EPI_SWIGLU || (g.N % (2 * g.granule) == 0));
 }
 
-cudaError_t gemv(const GemvArgs& g, cudaStream_t st) {
+cudaError_t gemv(const GemvArgs& g, int* /*dev_err: no bounded waits here*/, cudaStream_t st) {
     switch (g.M) {
         case 1: return gemv_launch<1>(g, st);
         case 2: return gemv_launch<2>(g, st);

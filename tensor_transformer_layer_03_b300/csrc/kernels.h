@@ -85,7 +85,7 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch
 typedef TcGemm GemvArgs;
 constexpr int GEMV_MAX_M = 8;
 bool gemv_supported(const GemvArgs& g);
-cudaError_t gemv(const GemvArgs& g, cudaStream_t st);
+cudaError_t gemv(const GemvArgs& g, int* dev_err, cudaStream_t st);
 
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
 bool tc_attention_supported(const AttnArgs& a);
@@ -94,7 +94,8 @@ cudaError_t tc_attention(const AttnArgs& a, int* dev_err, cudaStream_t st);
 
 // ---- single-token decode (decode.cu) ------------------------------------------
 // Split-KV attention: partial (max, sum, output) per key chunk in `scratch`
-// ([B][H][DECODE_MAX_SPLITS][dh + 2] floats), then a combine pass.
+// ([B][H][DECODE_MAX_SPLITS][dh + 2] floats), then a combine pass.  Also
+// writes the new token's K/V (from the QKV buffer) into the cache at pos.
 constexpr int DECODE_MAX_SPLITS = 64;
 cudaError_t decode_attention(const AttnArgs& a, float* scratch, cudaStream_t st);
 

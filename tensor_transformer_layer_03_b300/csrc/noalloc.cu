@@ -80,7 +80,6 @@ extern "C" tp_status tp_attention_decode_noalloc(tp_plan_t p, const void* qkv_sh
     a.causal = 1;
     a.scale = 1.0f / sqrtf((float)p->dh);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    e = tpk::kv_append(a, k_cache, v_cache, st);
-    if (e == cudaSuccess) e = tpk::decode_attention(a, scratch, st);
+    e = tpk::decode_attention(a, scratch, st);  // also appends the new token's K/V
     return tpk::status_from_cuda(e);
 }

@@ -218,7 +218,7 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
         g.out_shard = (long long)M * n_out;
         g.ldo = n_out;
         g.granule = p->granule;
-        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, st));
+        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, device_error_word(), st));
         if (tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32))
             return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
@@ -274,7 +274,7 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
         g.out2 = out_act;
         g.residual = residual;
         g.residual_f32 = res_f32;
-        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, st));
+        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, device_error_word(), st));
         if (tpk::tc_gemm_supported(M, p->d, ks))
             return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
@@ -334,7 +334,7 @@ tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int
     if (split_kv && !scratch) return TP_ERR_NULL_ARG;
     if (split_kv && scratch_bytes < need) return TP_ERR_WORKSPACE_TOO_SMALL;
     cudaError_t e = cudaSuccess;
-    if (cached) {
+    if (cached && !split_kv) {  // (the single-token path appends inside its kernels)
         e = tpk::kv_append(a, k_cache, v_cache, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
