@@ -260,7 +260,56 @@ def bench_decode(args, dev, flush):
     return {"workload": "llama7b_decode", "tp_degree": wl.tp, "batch": B, "cache_positions": P + 1,
             "us_per_step_median": med, "us_per_step_p10": sorted(us)[len(us) // 10],
             "algorithmic_bytes": algo, "gb_s": gbs, "hbm_peak_gb_s": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
-            "graph": True, "launches_per_step": 7, "l2": "flushed between steps"}
+            "graph": True, "launches_per_step": 6, "l2": "flushed between steps"}
+
+
+def run_sweep(args):
+    """One JSON line per workload of the batch x prompt sweep (7B shape, tp 4)
+    and of the tp sweep (13B shape, 4 x 1024 tokens): the whole block through
+    tp_block_forward, inputs resident, L2 flushed between steps, CUDA events."""
+    import torch
+
+    from tensor_transformer_layer_03_b300 import inputs as I
+    from tensor_transformer_layer_03_b300.runtime import TPBlock
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    pk = peaks()
+    wls = I.sweep_workloads() + [I.WORKLOADS["llama13b_b4t1024"].with_(name=f"llama13b_b4t1024_tp{t}", tp=t)
+                                 for t in I.TP_SWEEP]
+    st = torch.cuda.Stream(device=dev)
+    blk, key = None, None
+    for wl in wls:
+        gen = torch.Generator().manual_seed(0)
+        if key != (wl.shape, wl.tp):  # one set of packed weights per block shape and degree
+            blk = None
+            torch.cuda.empty_cache()
+            w = I.make_weights(wl.shape, wl.dtype, gen)
+            blk = TPBlock(wl.shape, wl.tp, wl.dtype, w, device=dev)
+            key = (wl.shape, wl.tp)
+            del w
+        blk.reserve(wl.batch, wl.seq)
+        x = torch.randn(wl.batch, wl.seq, wl.shape.d_model, generator=gen).to(torch.bfloat16).to(dev)
+        y = torch.empty(wl.batch, wl.seq, wl.shape.d_model, dtype=torch.float32, device=dev)
+        n = max(5, min(50, int(2e12 / sum(block_flops(wl)))))  # about 2 TFLOP of work per workload
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(st):
+            for i in range(3):
+                blk.forward(x, wl.causal, out=y, stream=st)
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                evs[i][0].record(st)
+                blk.forward(x, wl.causal, out=y, stream=st)
+                evs[i][1].record(st)
+            st.synchronize()
+        blk.plan.sync_status(st)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        lin, attn = block_flops(wl)
+        tf = (lin + attn) / (ms / 1e3) / 1e12
+        print(json.dumps({"workload": wl.name, "d_model": wl.shape.d_model, "tp_degree": wl.tp, "batch": wl.batch,
+                          "seq": wl.seq, "ms_per_block": ms, "tokens_per_s": wl.tokens / (ms / 1e3),
+                          "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "steps": n}), flush=True)
+        del x, y
+    return 0
 
 
 def run_ours(args):
@@ -426,11 +475,15 @@ def main():
     ap.add_argument("--workload", default="llama7b_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the headline line: one line per batch/prompt and tp-sweep workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

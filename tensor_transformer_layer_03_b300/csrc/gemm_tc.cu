@@ -58,6 +58,7 @@ struct GCfg {
     static constexpr int A_BYTES = A_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + W_ROWS * BK * 2;
     static constexpr int STAGES = PAIR ? TP_GEMM_PAIR_STAGES : 4;
+    static constexpr int GROUP_M = PAIR ? 8 : 16;       // row blocks per raster band (2048 rows)
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
     // instruction descriptor: D fp32, A/B bf16, both K-major
     static constexpr uint32_t IDESC = ptx::idesc_bf16(TILE_M, BN, false);
@@ -84,6 +85,23 @@ struct Params {
 };
 
 using namespace ptx;
+
+// Output tile t -> (row block, shard, column block).  Tiles run in bands of
+// `group_m` row blocks: inside a band the row block varies fastest, then the
+// column block (shard-major for column-parallel launches), so the tiles in
+// flight at once cover a compact rectangle and both the activation rows and
+// the weight rows they share stay in L2 even when M is large.
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int group_m, int& m_blk, int& shard, int& n_blk) {
+    const int nb = p.reduce ? p.n_blocks : p.n_blocks * p.shards;  // column tiles across shards
+    const int per_group = group_m * nb;
+    const int first_m = (t / per_group) * group_m;
+    const int gm = min(p.m_blocks - first_m, group_m);
+    const int r = t % per_group;
+    m_blk = first_m + r % gm;
+    const int nn = r / gm;
+    shard = p.reduce ? 0 : nn / p.n_blocks;
+    n_blk = p.reduce ? nn : nn % p.n_blocks;
+}
 
 // One unit's work: items w = unit, unit + n_units, ... of the sequence
 // (split-major, tile-minor, so units in flight together share k ranges and
@@ -187,10 +205,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             Seg g;
             while (ok && sc.next(g)) {
                 const int t = g.tile;
-                const int m_blk = t % p.m_blocks;
-                const int rest = t / p.m_blocks;
-                const int shard = p.reduce ? 0 : rest / p.n_blocks;
-                const int n_blk = p.reduce ? rest : rest % p.n_blocks;
+                int m_blk, shard, n_blk;
+                tile_coords(p, t, C::GROUP_M, m_blk, shard, n_blk);
                 const int a_row = m_blk * C::TILE_M + (int)rank * A_ROWS;
                 const int w_row = n_blk * BN + (int)rank * C::W_ROWS;
                 for (int kb = g.k0; kb < g.k1; ++kb) {
@@ -302,10 +318,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
             if (!mbar_wait_warp(&tmem_full[buf], acc_phase, abort_flag, p.err, p.timeout_ns)) break;
             tc_fence_after();
-            const int m_blk = t % p.m_blocks;
-            const int rest = t / p.m_blocks;
-            const int shard = p.reduce ? 0 : rest / p.n_blocks;
-            const int n_blk = p.reduce ? rest : rest % p.n_blocks;
+            int m_blk, shard, n_blk;
+            tile_coords(p, t, C::GROUP_M, m_blk, shard, n_blk);
             const int row = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
             const int col_base = n_blk * BN;
