@@ -45,7 +45,7 @@ using namespace ptx;
 
 constexpr int AT_ROWS = 128;   // query rows per tile (MMA M)
 constexpr int AT_KEYS = 128;   // keys per step (MMA N of S, K of P V)
-constexpr int AT_SLOTS = 3;    // K/V ring slots
+constexpr int AT_SLOTS = 5;    // K/V ring slots
 constexpr int AT_THREADS = 320;
 constexpr int HALF_BYTES = 128 * 64 * 2;  // one 128-row x 64-column swizzled half tile
 constexpr float RESCALE_LOG2 = 8.0f;      // rescale O only when the max grows by > 2^8
@@ -54,11 +54,9 @@ constexpr unsigned long long AT_TIMEOUT_NS = 2000000000ull;
 template <int D>
 struct Cfg {
     static constexpr int TILE = 128 * D * 2;  // a Q, K or V tile: D/64 halves
-    static constexpr int P_TILE = 128 * AT_KEYS * 2;
     static constexpr int Q_OFF = 0;
     static constexpr int RING_OFF = Q_OFF + 2 * TILE;
-    static constexpr int P_OFF = RING_OFF + AT_SLOTS * TILE;
-    static constexpr int BAR_OFF = P_OFF + 2 * P_TILE;
+    static constexpr int BAR_OFF = RING_OFF + AT_SLOTS * TILE;
     static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
 };
@@ -148,7 +146,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t sQ = smem_u32(smem + C::Q_OFF);
     const uint32_t sRing = smem_u32(smem + C::RING_OFF);
-    const uint32_t sP = smem_u32(smem + C::P_OFF);
 
     // column of head jl's Q / K / V in a QKV row, and the map coordinates
     const int rowq = jl * D;
@@ -191,63 +188,64 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(AT_ROWS, AT_KEYS, false);
             constexpr uint32_t IDESC_O = idesc_bf16(AT_ROWS, D, true);
+            const int nkt0 = nkt(0), nkt1 = nkt(1);
+            // descriptor bases; the start-address field counts 16-byte units,
+            // so a byte offset o inside the tile is + (o >> 4)
+            const uint64_t dq0 = sw128_desc(sQ, 16, 1024), dq1 = sw128_desc(sQ + C::TILE, 16, 1024);
+            const uint64_t dk = sw128_desc(sRing, 16, 1024);              // K tiles: K-major over d_head
+            const uint64_t dv = sw128_desc(sRing, HALF_BYTES, 1024);      // V tiles: MN-major (d_head)
             bool ok = mbar_wait(q_full, 0, abort_flag, p.err, p.timeout_ns);
             tc_fence_after();
             int kv_seen = -1;  // ring items known to have landed
-            auto need_item = [&](int i) -> bool {
-                while (kv_seen < i) {
-                    const int n = kv_seen + 1;
-                    if (!mbar_wait(&kv_full[n % AT_SLOTS], (uint32_t)(n / AT_SLOTS) & 1u, abort_flag, p.err,
-                                   p.timeout_ns))
-                        return false;
-                    tc_fence_after();
-                    kv_seen = n;
-                }
-                return true;
-            };
-            auto issue_s = [&](int t, int j) {
-                const uint32_t ks = sRing + (uint32_t)((2 * j) % AT_SLOTS) * C::TILE;
-                const uint32_t qs = sQ + t * C::TILE;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_f16(tmem_base + t * AT_KEYS, kmajor_desc(qs, kk * 16), kmajor_desc(ks, kk * 16), IDESC_S,
-                             kk > 0 ? 1u : 0u);
-                umma_commit(&s_full[t]);
-                if (t == last_t) umma_commit(&kv_empty[(2 * j) % AT_SLOTS]);
-            };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t vs = sRing + (uint32_t)((2 * j + 1) % AT_SLOTS) * C::TILE;
-                const uint32_t ps = sP + t * C::P_TILE;
-                const uint32_t o_t = tmem_base + 2 * AT_KEYS + t * D;
-#pragma unroll
-                for (int kk = 0; kk < AT_KEYS / 16; ++kk)
-                    umma_f16(o_t, kmajor_desc(ps, kk * 16), sw128_desc(vs + kk * 16 * 128, HALF_BYTES, 1024), IDESC_O,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-                if (t == last_t) umma_commit(&kv_empty[(2 * j + 1) % AT_SLOTS]);
-                if (j == nkt(t) - 1) umma_commit(&o_full[t]);
-            };
-            if (ok && n_kt > 0) {
-                ok = need_item(0);
-                for (int t = 0; t < 2 && ok; ++t)
-                    if (nkt(t) > 0) issue_s(t, 0);
-            }
-            for (int j = 0; j < n_kt && ok; ++j) {
+            // step -1 issues S_t(0); step j >= 0 issues P V_t(j) then S_t(j+1), t = 0, 1
+            for (int j = -1; j < n_kt && ok; ++j) {
+#pragma unroll 1
                 for (int t = 0; t < 2 && ok; ++t) {
-                    if (j < nkt(t)) {
-                        if (!need_item(2 * j + 1) ||
-                            !mbar_wait(&p_full[t], (uint32_t)j & 1u, abort_flag, p.err, p.timeout_ns)) {
-                            ok = false;
-                            break;
+                    const int nk = t ? nkt1 : nkt0;
+                    if (j >= 0 && j < nk) {
+                        // P V_t(j): P from TMEM (bf16 pairs over the first half of S_t)
+                        const int item = 2 * j + 1;
+                        while (ok && kv_seen < item) {
+                            const int n = kv_seen + 1;
+                            ok = mbar_wait(&kv_full[n % AT_SLOTS], (uint32_t)(n / AT_SLOTS) & 1u, abort_flag, p.err,
+                                           p.timeout_ns);
+                            kv_seen = n;
                         }
+                        ok = ok && mbar_wait(&p_full[t], (uint32_t)j & 1u, abort_flag, p.err, p.timeout_ns);
+                        if (!ok) break;
                         tc_fence_after();
-                        issue_pv(t, j);
+                        const int slot = item % AT_SLOTS;
+                        const uint64_t vd = dv + (uint64_t)((slot * C::TILE) >> 4);
+                        const uint32_t p_t = tmem_base + t * AT_KEYS;
+                        const uint32_t o_t = tmem_base + 2 * AT_KEYS + t * D;
+#pragma unroll
+                        for (int kk = 0; kk < AT_KEYS / 16; ++kk)
+                            umma_f16_ta(o_t, p_t + kk * 8, vd + (uint64_t)(kk * 128), IDESC_O,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                        if (t == last_t) umma_commit(&kv_empty[slot]);
+                        if (j == nk - 1) umma_commit(&o_full[t]);
                     }
-                    if (j + 1 < nkt(t)) {
-                        if (!need_item(2 * (j + 1))) {
-                            ok = false;
-                            break;
+                    if (j + 1 < nk) {
+                        // S_t(j+1) = Q_t K_{j+1}^T
+                        const int item = 2 * (j + 1);
+                        while (ok && kv_seen < item) {
+                            const int n = kv_seen + 1;
+                            ok = mbar_wait(&kv_full[n % AT_SLOTS], (uint32_t)(n / AT_SLOTS) & 1u, abort_flag, p.err,
+                                           p.timeout_ns);
+                            kv_seen = n;
                         }
-                        issue_s(t, j + 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const int slot = item % AT_SLOTS;
+                        const uint64_t kd = dk + (uint64_t)((slot * C::TILE) >> 4);
+                        const uint64_t qd = t ? dq1 : dq0;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t off = (uint64_t)((kk / 4) * (HALF_BYTES >> 4) + (kk % 4) * 2);
+                            umma_f16(tmem_base + t * AT_KEYS, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&s_full[t]);
+                        if (t == last_t) umma_commit(&kv_empty[slot]);
                     }
                 }
             }
@@ -275,7 +273,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const uint32_t tO = tmem_base + lane_off + 2 * AT_KEYS + t * D;
             const int qpos = p.pos + q0t + row;          // absolute position of this query
             const int warp_qmin = p.pos + q0t + quarter * 32;
-            const uint32_t prow = sP + t * C::P_TILE + row * 128;
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nkt_t; ++j) {
@@ -284,8 +281,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                // raw scores; the scale is folded into the exponent below:
-                // p = 2^(s * scale * log2(e) - m), m kept in scaled units
+                // this row of S, all 128 columns in one TMEM round trip; scores
+                // stay raw, the scale is folded into the exponent below
                 float sv[AT_KEYS];
                 {
                     uint32_t r[4][32];
@@ -300,12 +297,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 const int k0 = j * AT_KEYS;
                 const bool masked = (k0 + AT_KEYS > p.nkeys) || (p.causal && k0 + AT_KEYS - 1 > warp_qmin);
                 if (masked) {
-                    const int lim = p.causal ? min(p.nkeys - 1, qpos) : p.nkeys - 1;  // last visible key
+                    const int lim = (p.causal ? min(p.nkeys - 1, qpos) : p.nkeys - 1) - k0;  // last visible column
 #pragma unroll
                     for (int i = 0; i < AT_KEYS; ++i)
-                        if (k0 + i > lim) sv[i] = -INFINITY;
+                        if (i > lim) sv[i] = -INFINITY;
                 }
-                // row max over 8 independent chains, then a short tree
                 float m8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) m8[i] = sv[i];
@@ -317,9 +313,32 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 // keep the stale max unless the row max grew by more than 2^8
                 const bool grow = j == 0 || mx > m_used + RESCALE_LOG2;
                 const float m_new = grow ? fmaxf(m_used, mx) : m_used;
-                if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                    const float corr = grow ? ex2(m_used - m_new) : 1.f;
-                    l *= corr;
+                const float corr = (j > 0 && grow) ? ex2(m_used - m_new) : 1.f;
+                m_used = m_new;
+                const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+                float rs8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+                // P = 2^(s - m) as bf16 pairs written back over the first 64
+                // columns of this row of S (in registers already), where the
+                // P V product reads its A operand
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float e0 = ex2(fmaf(sv[32 * q + 2 * i], p.scale_log2, neg_m));
+                        const float e1 = ex2(fmaf(sv[32 * q + 2 * i + 1], p.scale_log2, neg_m));
+                        rs8[(2 * i) & 7] += e0;
+                        rs8[(2 * i + 1) & 7] += e1;
+                        pk[i] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st16u(tS + 16 * q, pk);
+                }
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                // the scores are dead here: rescale this row of O (rare) before
+                // the next P V accumulates into it
+                if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         float ov[32];
@@ -330,30 +349,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     }
                     tmem_st_wait();
                 }
-                m_used = m_new;
-                const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-                float rs8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll
-                for (int c = 0; c < AT_KEYS / 8; ++c) {
-                    float e[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        e[i] = ex2(fmaf(sv[8 * c + i], p.scale_log2, neg_m));
-                        rs8[i] += e[i];
-                    }
-                    const uint4 v = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                                               pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
-                    const int half = c / 8, chunk = c % 8;
-                    const uint32_t addr = prow + half * HALF_BYTES + (uint32_t)((chunk ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                                 "r"(v.z), "r"(v.w)
-                                 : "memory");
-                }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                l = l * corr;
                 l += rs;
-                fence_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[t]);
