@@ -402,33 +402,60 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
                 "peak_source": f"{pk['source']} bf16 dense burst (cuBLAS)"}
 
-    # end to end through the public call: pinned host x in, Y out
+    # end to end through the public call: every step copies its input X from
+    # pinned host memory and reads its output Y back to pinned host memory.
+    # Copy-in, compute and copy-out run on three streams with double-buffered
+    # device tensors, so step i's copies overlap steps i-1 / i+1's compute;
+    # every step's two copies are inside the timed region.  No L2 flush: the
+    # weights and activations a step touches (~0.6 GB) exceed the 126 MB L2.
+    e2e = None
     if True:
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         xh = x.cpu().pin_memory()
-        yh = torch.empty(M, d, dtype=torch.float32).pin_memory()
-        xd = torch.empty_like(x)
-        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                xd.copy_(xh, non_blocking=True)
-                blk.forward(xd, wl.causal, out=y.view(B, T, d), stream=stream)
-                yh.copy_(y, non_blocking=True)
-            stream.synchronize()
-            tot = 0.0
-            for i in range(args.steps):
-                flush.fill_(i & 0xFF)
-                e0[i].record(stream)
-                xd.copy_(xh, non_blocking=True)
-                blk.forward(xd, wl.causal, out=y.view(B, T, d), stream=stream)
-                yh.copy_(y, non_blocking=True)
-                e0[i + 1].record(stream)
-                stream.synchronize()
-                tot += e0[i].elapsed_time(e0[i + 1])
+        yh = [torch.empty(M, d, dtype=torch.float32).pin_memory() for _ in range(2)]
+        xd = [torch.empty_like(x) for _ in range(2)]
+        yd = [torch.empty(B, T, d, dtype=torch.float32, device=dev) for _ in range(2)]
+
+        def pipelined(n):
+            ev = lambda: torch.cuda.Event()
+            in_done, comp_done, out_done = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
+            for i in range(n):
+                k = i & 1
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(comp_done[i - 2])  # xd[k] consumed
+                    xd[k].copy_(xh, non_blocking=True)
+                    in_done[i].record(s_in)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(in_done[i])
+                    if i >= 2:
+                        stream.wait_event(out_done[i - 2])  # yd[k] read back
+                    blk.forward(xd[k], wl.causal, out=yd[k], stream=stream)
+                    comp_done[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp_done[i])
+                    yh[k].copy_(yd[k].view(M, d), non_blocking=True)
+                    out_done[i].record(s_out)
+            return out_done[-1]
+
+        pipelined(args.warmup)
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        s_in.wait_event(t_start)
+        last = pipelined(args.steps)
+        stream.wait_event(last)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
         plan.sync_status(stream)
-        tot = max_over_ranks(tot, pg, dev)
+        tot = max_over_ranks(t_start.elapsed_time(t_end), pg, dev)
         e2e = {"value": M * args.steps * world / (tot / 1000.0), "unit": "tokens/s",
-               "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": y.numel() * 4,
-               "ms_per_step": tot / args.steps}
+               "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": M * d * 4,
+               "ms_per_step": tot / args.steps, "pipelined": "copy-in / compute / copy-out streams, double buffers",
+               "l2": "no flush; a step touches ~0.6 GB (> 126 MB L2)"}
 
     decode = bench_decode(args, dev, flush) if not args.no_decode else None
 
