@@ -233,105 +233,141 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_split_bf16_k(AttnArgs a, f
     }
 }
 
-// bf16 single-token pass 1, latency-lean: one block per (sequence, head,
-// chunk of 64 keys).  Every thread issues all of its K and V loads up front
-// (a key row is split between two threads), so a chunk costs one memory
-// round trip; the new token's K/V row (position pos) is read from the QKV
-// buffer and written into the cache by the block that owns it, so no
-// separate append pass runs.  Scores in log2 units; partial (m, l, o) as in
-// the kernels above.
+// bf16 single-token pass 1: one block (4 warps) per (sequence, head, chunk
+// of 64 keys), 16 keys per warp.  Loads are coalesced: in each load
+// instruction a warp reads 512 contiguous bytes of the K (then V) cache,
+// i.e. KPI whole key rows, one 16-byte chunk (8 dimensions) per lane; every
+// K and V load of the chunk is issued before any is used, so a chunk costs
+// one memory round trip.  A lane keeps q for its 8 dimensions; a key's score
+// is reduced over the CH lanes that hold its row (shuffles), P V is summed in
+// registers over the warp's keys and across the 4 warps in shared memory.
+// The new token's K/V row (position pos) comes from the QKV buffer and is
+// written into the cache here, so no separate append pass runs.  Scores in
+// log2 units; partial (m, l, o) as in the kernels above.
 constexpr int DC_KEYS = 64;
 
 template <int DH>
 __global__ void __launch_bounds__(DEC_THREADS) decode_chunk_bf16_k(AttnArgs a, float* __restrict__ part) {
-    constexpr int CH = DH / 8;        // 16-byte chunks per key row
-    constexpr int CPT = CH / 2;       // chunks per thread (half a row)
-    constexpr int G = DEC_THREADS / DH;
-    __shared__ float qs[DH];
-    __shared__ __align__(16) bf16 vs[DC_KEYS][DH];
-    __shared__ float ps[DC_KEYS];
-    __shared__ float red[DEC_THREADS / 32];
-    __shared__ float ored[G][DH];
+    constexpr int CH = DH / 8;           // 16-byte chunks per key row (16 or 8)
+    constexpr int KPI = 32 / CH;         // key rows per warp load instruction
+    constexpr int NW = DEC_THREADS / 32;
+    constexpr int KPW = DC_KEYS / NW;    // keys per warp
+    constexpr int NI = KPW / KPI;        // load instructions per warp and matrix
+    __shared__ float red[2][NW];
+    __shared__ float ored[NW][DH];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int s = h / a.hl, jl = h % a.hl;
-    const int t = threadIdx.x;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int ch = lane % CH, r = lane / CH;  // this lane's 8 dimensions, and which row of the instruction
     const int L = a.pos + 1;
-    const int k0 = c * DC_KEYS;
-    const int key = k0 + t / 2, half = t % 2;
-    const bool have = key < L;
+    const int kw = c * DC_KEYS + warp * KPW;  // first key of this warp
     const bf16* qkv_row = (const bf16*)a.qkv + ((long long)s * a.B + b) * (3 * a.hl * DH);
     bf16* kcache = (bf16*)a.kc + ((long long)b * a.H + h) * a.cap * DH;
     bf16* vcache = (bf16*)a.vc + ((long long)b * a.H + h) * a.cap * DH;
     // everything read below (Q, the new K/V, and cache rows appended by
     // earlier steps' kernels) may come from kernels still finishing
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    uint4 kv[CPT], vv[CPT];
-    const bool is_new = key == a.pos;
-    if (have && !is_new) {
+    uint4 kv[NI], vv[NI];
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            kv[i] = reinterpret_cast<const uint4*>(kcache + (long long)key * DH)[half * CPT + i];
-            vv[i] = reinterpret_cast<const uint4*>(vcache + (long long)key * DH)[half * CPT + i];
+    for (int i = 0; i < NI; ++i) {
+        const int key = kw + i * KPI + r;
+        kv[i] = vv[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (key < L && key != a.pos) {
+            kv[i] = reinterpret_cast<const uint4*>(kcache + (long long)key * DH)[ch];
+            vv[i] = reinterpret_cast<const uint4*>(vcache + (long long)key * DH)[ch];
         }
     }
-    if (is_new) {
-        const uint4* kn = reinterpret_cast<const uint4*>(qkv_row + (a.hl + jl) * DH) + half * CPT;
-        const uint4* vn = reinterpret_cast<const uint4*>(qkv_row + (2 * a.hl + jl) * DH) + half * CPT;
+    float q[8];
+    {
+        const uint4 qv = reinterpret_cast<const uint4*>(qkv_row + jl * DH)[ch];
+        const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&qv);
+        const float sl2 = a.scale * 1.4426950408889634f;
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            kv[i] = kn[i];
-            vv[i] = vn[i];
-            reinterpret_cast<uint4*>(kcache + (long long)key * DH)[half * CPT + i] = kv[i];
-            reinterpret_cast<uint4*>(vcache + (long long)key * DH)[half * CPT + i] = vv[i];
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(hq[e]);
+            q[2 * e] = f.x * sl2;
+            q[2 * e + 1] = f.y * sl2;
         }
     }
-    const float sl2 = a.scale * 1.4426950408889634f;
-    for (int i = t; i < DH; i += DEC_THREADS) qs[i] = __bfloat162float(qkv_row[jl * DH + i]) * sl2;
+    // the new token's row: from the QKV buffer, and into the cache
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const int key = kw + i * KPI + r;
+        if (key == a.pos) {
+            kv[i] = reinterpret_cast<const uint4*>(qkv_row + (a.hl + jl) * DH)[ch];
+            vv[i] = reinterpret_cast<const uint4*>(qkv_row + (2 * a.hl + jl) * DH)[ch];
+            reinterpret_cast<uint4*>(kcache + (long long)key * DH)[ch] = kv[i];
+            reinterpret_cast<uint4*>(vcache + (long long)key * DH)[ch] = vv[i];
+        }
+    }
+    // scores of this lane's NI keys (equal across the CH lanes of a row)
+    float sc[NI];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&kv[i]);
+        float d = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(hk[e]);
+            d = fmaf(q[2 * e], f.x, d);
+            d = fmaf(q[2 * e + 1], f.y, d);
+        }
+#pragma unroll
+        for (int off = CH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        sc[i] = (kw + i * KPI + r < L) ? d : -INFINITY;
+        mx = fmaxf(mx, sc[i]);
+    }
+#pragma unroll
+    for (int off = CH; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[0][warp] = mx;
     __syncthreads();
-    // score of this thread's key: its half-row dot q, then the partner's half
-    float d = 0.f;
-    if (have) {
+    float m = red[0][0];
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&kv[i]);
+    for (int w2 = 1; w2 < NW; ++w2) m = fmaxf(m, red[0][w2]);
+    // p and the running sums; o over this lane's keys and 8 dimensions
+    float l = 0.f, o[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(hk[e]);
-                const int dim = (half * CPT + i) * 8 + 2 * e;
-                d = fmaf(qs[dim], f.x, d);
-                d = fmaf(qs[dim + 1], f.y, d);
-            }
+    for (int e = 0; e < 8; ++e) o[e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const float pr = exp2f(sc[i] - m);  // 0 for keys past the end (-inf)
+        l += pr;
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&vv[i]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(hv[e]);
+            o[2 * e] = fmaf(pr, f.x, o[2 * e]);
+            o[2 * e + 1] = fmaf(pr, f.y, o[2 * e + 1]);
         }
     }
-    d += __shfl_xor_sync(0xffffffffu, d, 1);
-    const float sc = have ? d : -INFINITY;
-    if (have) {
+    // sum over the rows of the warp (lanes with the same chunk), then warps
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) reinterpret_cast<uint4*>(&vs[t / 2][0])[half * CPT + i] = vv[i];
+    for (int off = CH; off < 32; off <<= 1) {
+        l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] += __shfl_xor_sync(0xffffffffu, o[e], off);
     }
-    const float m = block_reduce(sc, red, true);
-    const float pr = have ? exp2f(sc - m) : 0.f;
-    if (half == 0) ps[t / 2] = pr;
-    const float l = block_reduce(half == 0 ? pr : 0.f, red, false);  // its barriers publish ps[] and vs[]
-    // o[dim] = sum_k p_k v[k][dim]; G key groups per dimension
-    const int dim = t % DH, grp = t / DH;
-    const int nk = min(DC_KEYS, L - k0);
-    float o = 0.f;
-#pragma unroll 8
-    for (int k = grp; k < nk; k += G) o = fmaf(ps[k], __bfloat162float(vs[k][dim]), o);
-    ored[grp][dim] = o;
+    if (r == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ored[warp][ch * 8 + e] = o[e];
+    }
+    if (lane == 0) red[1][warp] = l;
     __syncthreads();
     float* dst = part + (((long long)b * a.H + h) * DECODE_MAX_SPLITS + c) * (DH + 2);
-    if (t < DH) {
+    for (int i = threadIdx.x; i < DH; i += DEC_THREADS) {
         float acc = 0.f;
 #pragma unroll
-        for (int g2 = 0; g2 < G; ++g2) acc += ored[g2][t];
-        dst[2 + t] = acc;
+        for (int w2 = 0; w2 < NW; ++w2) acc += ored[w2][i];
+        dst[2 + i] = acc;
     }
-    if (t == 0) {
+    if (threadIdx.x == 0) {
+        float lt = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2) lt += red[1][w2];
         dst[0] = m;
-        dst[1] = l;
+        dst[1] = lt;
     }
 }
 

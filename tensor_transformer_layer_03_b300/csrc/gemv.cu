@@ -2,11 +2,16 @@
 //
 // With one to a few tokens per step every weight element is used M times, so
 // the linears are bound by reading the packed weights once from HBM.  Each
-// warp owns whole weight rows and streams them with 16-byte non-allocating
-// loads, eight in flight per lane; the M input rows are read through the
-// read-only cache (every warp of the GPU reads the same few KB, so they stay
-// in L1/L2).  Kernels are specialised on the number of token rows so the
-// registers go to loads in flight, not to unused accumulators.
+// warp owns whole work items and streams two weight rows at a time with
+// 16-byte non-allocating loads (16 in flight per lane); the M input rows are
+// read through the read-only cache (every warp of the GPU reads the same few
+// KB, so they stay in L1/L2).  Kernels are specialised on the number of token
+// rows so the registers go to loads in flight, not to unused accumulators.
+// The grid gives every warp the same number of items with all blocks
+// resident at once.  Launches allow programmatic dependent launch: a kernel
+// lets the next one start at entry and waits (griddepcontrol.wait) for the
+// previous one before reading its input rows, so launch latency and block
+// start-up overlap the previous kernel's tail.
 //
 //  * column-parallel (undercodenews.com/?p=110319, "the Original": every
 //    shard multiplies the full input by its slice of the output features):
@@ -49,15 +54,12 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
     return s;
 }
 
-// Start pulling `bytes` (a multiple of 16) at p into L2 without waiting.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 // Programmatic dependent launch: let the next kernel in the stream start
 // (it waits for this one before reading its outputs) / wait for the
 // previous kernel's results.  No-ops when the launch did not allow it.
 __device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -133,23 +135,6 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
     const bf16* W = (const bf16*)g.W;
     const bf16* X = (const bf16*)g.A;
     pdl_launch_next();
-    // the packed weights are written only by the packing kernels, never by a
-    // kernel this one can overlap: start this warp's first rows toward L2
-    // before waiting for the input rows
-    if (lane == 0) {
-        const uint32_t row_bytes = (uint32_t)g.K * 2;
-        if (EPI == EPI_SWIGLU) {
-            const int n_out = g.N / 2;
-            if (gw < g.shards * n_out) {
-                const int s = gw / n_out, j = gw % n_out;
-                const long long gate_row = (long long)s * g.N + (j / g.granule) * 2 * g.granule + j % g.granule;
-                prefetch_l2(W + gate_row * g.K, row_bytes);
-                prefetch_l2(W + (gate_row + g.granule) * g.K, row_bytes);
-            }
-        } else if (gw < g.shards * g.N) {
-            prefetch_l2(W + (long long)gw * g.K, row_bytes);
-        }
-    }
     pdl_wait_prev();
     if (EPI == EPI_SWIGLU) {
         const int n_out = g.N / 2;  // U columns per shard
@@ -205,8 +190,6 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_row_k(GemvArgs g) {
     const bf16* W = (const bf16*)g.W;
     const bf16* A = (const bf16*)g.A;
     pdl_launch_next();
-    if (lane == 0 && gw < g.N)  // first output row's weights, every shard (see gemv_col_k)
-        for (int s = 0; s < g.shards; ++s) prefetch_l2(W + s * g.w_shard + (long long)gw * g.K, (uint32_t)g.K * 2);
     pdl_wait_prev();
     for (int n = gw; n < g.N; n += nw) {
         float acc[MT];
