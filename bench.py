@@ -207,15 +207,17 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def bench_decode(args, dev, flush):
+def bench_decode(args, dev, flush=None, batch=1, timeline=False):
     """One-token decode step of the 7B-shaped block (tp 2, 1024 cached
-    positions + the new one), captured in a CUDA graph; HBM GB/s against the
-    algorithmic bytes (every packed weight once + the K/V cache read)."""
+    positions + the new one) for `batch` sequences, captured in a CUDA graph;
+    HBM GB/s against the algorithmic bytes (every packed weight once + the
+    K/V cache read).  With `timeline`, also the device start/end of every
+    kernel of one replay (CUPTI through torch.profiler)."""
     import torch
 
     from tensor_transformer_layer_03_b300 import inputs as I
     from tensor_transformer_layer_03_b300.runtime import TPBlock
-    wl = I.WORKLOADS["llama7b_decode"]
+    wl = I.WORKLOADS["llama7b_decode"].with_(batch=batch)
     inp = I.make_inputs(wl, seed=0)
     w = {k: v for k, v in inp.items() if k.startswith("W")}
     s = wl.shape
@@ -243,12 +245,24 @@ def bench_decode(args, dev, flush):
         for i in range(3):
             graph.replay()
         for i in range(n):
-            # no flush: a step streams 421.5 MB (> 126 MB L2), so nothing a
-            # step reads can still be in L2 from the step before it
+            # no flush: a step streams the packed weights (405 MB) and the
+            # cache (> 126 MB L2), so nothing it reads survives in L2
             evs[i][0].record(st)
             graph.replay()
             evs[i][1].record(st)
         st.synchronize()
+        tl = None
+        if timeline:
+            from torch.profiler import ProfilerActivity, profile
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                for i in range(3):
+                    graph.replay()
+                st.synchronize()
+            ks = sorted((e.time_range.start, e.time_range.end, e.name) for e in prof.events()
+                        if e.device_type.name == "CUDA")[-6:]
+            t0 = ks[0][0]
+            tl = [{"kernel": n.replace("(anonymous namespace)::", "").replace("void ", "").split("(")[0],
+                   "start_us": round(a - t0, 2), "end_us": round(b - t0, 2)} for a, b, n in ks]
     blk.plan.sync_status(st)
     us = [a.elapsed_time(b) * 1000.0 for a, b in evs]
     d, f = s.d_model, s.d_ffn
@@ -261,8 +275,9 @@ def bench_decode(args, dev, flush):
     return {"workload": "llama7b_decode", "tp_degree": wl.tp, "batch": B, "cache_positions": P + 1,
             "us_per_step_median": med, "us_per_step_p10": sorted(us)[len(us) // 10],
             "algorithmic_bytes": algo, "gb_s": gbs, "hbm_peak_gb_s": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
-            "graph": True, "launches_per_step": 6,
-            "l2": "not flushed: each step streams 421.5 MB of weights and cache (> 126 MB L2)"}
+            "tokens_per_s": B / (med * 1e-6), "graph": True, "launches_per_step": 6,
+            "l2": f"not flushed: each step streams {algo / 1e6:.1f} MB of weights and cache (> 126 MB L2)",
+            **({"timeline": tl} if tl else {})}
 
 
 def run_sweep(args):
@@ -311,6 +326,40 @@ def run_sweep(args):
                           "seq": wl.seq, "ms_per_block": ms, "tokens_per_s": wl.tokens / (ms / 1e3),
                           "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "steps": n}), flush=True)
         del x, y
+    blk = None
+    torch.cuda.empty_cache()
+    # a stack of 4 7B-shaped layers (tp 4), prefill of 1 x 2048 tokens
+    from tensor_transformer_layer_03_b300.runtime import TPStack
+    wl = I.WORKLOADS["llama7b_prefill"]
+    gen = torch.Generator().manual_seed(0)
+    stk = TPStack(wl.shape, wl.tp, wl.dtype, [I.make_weights(wl.shape, wl.dtype, gen) for _ in range(4)],
+                  device=dev, max_batch=wl.batch, max_seq=wl.seq)
+    x = torch.randn(wl.batch, wl.seq, wl.shape.d_model, generator=gen).to(torch.bfloat16).to(dev)
+    y = torch.empty(wl.batch, wl.seq, wl.shape.d_model, dtype=torch.float32, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    with torch.cuda.stream(st):
+        for i in range(3):
+            stk.forward(x, True, out=y, stream=st)
+        for i in range(10):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(st)
+            stk.forward(x, True, out=y, stream=st)
+            evs[i][1].record(st)
+        st.synchronize()
+    stk.plan.sync_status(st)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    lin, attn = block_flops(wl)
+    tf = 4 * (lin + attn) / (ms / 1e3) / 1e12
+    print(json.dumps({"workload": "llama7b_stack4_b1_t2048", "layers": 4, "tp_degree": wl.tp, "ms_per_stack": ms,
+                      "tokens_per_s": wl.tokens / (ms / 1e3), "tflops": tf,
+                      "frac_of_bf16_peak": tf / pk["bf16_tflops"]}), flush=True)
+    del stk, x, y
+    torch.cuda.empty_cache()
+    # batched one-token decode at 1024 cached positions (7B shape, tp 2)
+    for b in (1, 4, 16, 64):
+        r = bench_decode(args, dev, batch=b)
+        print(json.dumps({"workload": f"llama7b_decode_b{b}", **r}), flush=True)
+        torch.cuda.empty_cache()
     return 0
 
 
@@ -462,7 +511,7 @@ def run_ours(args):
                "ms_per_step": tot / args.steps, "pipelined": "copy-in / compute / copy-out streams, double buffers",
                "l2": "no flush; a step touches ~0.6 GB (> 126 MB L2)"}
 
-    decode = bench_decode(args, dev, flush) if not args.no_decode else None
+    decode = bench_decode(args, dev) if not args.no_decode else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -507,6 +556,10 @@ def main():
     ap.add_argument("--workload", default="llama7b_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="instead of the headline line: only the decode leg (for profiling its kernels)")
+    ap.add_argument("--decode-batch", type=int, default=1)
+    ap.add_argument("--timeline", action="store_true", help="with --decode-only: per-kernel device timeline")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline line: one line per batch/prompt and tp-sweep workload")
     args = ap.parse_args()
@@ -516,6 +569,11 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.decode_only:
+        import torch
+        print(json.dumps(bench_decode(args, torch.device("cuda", 0), batch=args.decode_batch,
+                                      timeline=args.timeline)), flush=True)
+        return 0
     return run_ours(args)
 
 

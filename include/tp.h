@@ -245,6 +245,26 @@ tp_status tp_block_forward(tp_plan_t plan, const void* x, int batch, int seq, in
                            void* out_f32, void* stream);
 
 /*
+ * A stack of n_layers blocks of the plan's shape (each with its own packed
+ * weights and, optionally, its own KV cache), the output of layer l feeding
+ * layer l + 1 -- the layers a device_map or pipeline split would place on
+ * different GPUs (undercodenews "device-map-vs-tensor-parallelism-exposed",
+ * "the Original"; undercodenews.com/?p=110319), here all tensor-parallel on
+ * one GPU.  Between layers the activation is stored in the plan dtype (the
+ * next layer's input is the plan-dtype copy of the previous layer's Y);
+ * out_f32 receives the last layer's Y.
+ *   packed_layers  host array of n_layers device pointers (tp_shard_weights)
+ *   k_caches, v_caches  host arrays of n_layers device caches (as in
+ *                  tp_attention_heads) or both NULL
+ *   workspace      device, ws_bytes >= tp_stack_workspace_bytes(batch, seq)
+ */
+tp_status tp_stack_workspace_bytes(tp_plan_t plan, int batch, int seq, size_t* bytes);
+tp_status tp_stack_forward(tp_plan_t plan, int n_layers, const void* const* packed_layers, const void* x,
+                           int batch, int seq, int causal, void* const* k_caches, void* const* v_caches,
+                           int cache_cap, int cache_pos, void* workspace, size_t ws_bytes, void* out_f32,
+                           void* stream);
+
+/*
  * Wait for `stream`, then report (and clear) the first device-side error
  * recorded by a bounded wait in this library's kernels on the current
  * device: TP_ERR_DEVICE_TIMEOUT, TP_ERR_CUDA on a CUDA error, else TP_OK.

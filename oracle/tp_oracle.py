@@ -25,6 +25,10 @@ Sources (cited by page title and section):
 * [BYTE] "Tensor Parallelism: Splitting One Layer Across GPUs" (byteledger),
   section "Interaction with the rest of serving": the KV cache is split along
   with the heads.
+* [DMAP] undercodenews "device-map-vs-tensor-parallelism-exposed", section
+  "the Original": a model is a sequence of layers, each consuming the
+  previous layer's output; device_map places whole layers on different
+  devices, tensor parallelism splits every layer.
 
 Readings where the pages are silent (each is listed with its reason in the
 design notes):
@@ -41,7 +45,9 @@ design notes):
 * the all-reduce sums the partials in shard order s = 0..tp-1;
 * ``storage="bf16"`` rounds (round-to-nearest-even) the tensors that the
   bf16 data path stores between steps: Q/K/V, the attention output, the bf16
-  operand copy of H and U; H itself is kept in fp32 for the residual.
+  operand copy of H and U; H itself is kept in fp32 for the residual;
+* in a stack of layers the activation passed from one layer to the next is
+  stored in the plan dtype (``act_dtype``), in both storage modes.
 
 Arrays may be numpy arrays or torch CPU tensors of any float dtype; every
 function returns float64 numpy arrays.
@@ -58,7 +64,7 @@ __all__ = [
     "linear", "gelu_erf", "silu", "softmax_rows", "attention_head",
     "multi_head_attention", "column_parallel_linear", "row_parallel_partials",
     "all_reduce_sum", "ffn", "block_forward", "sharded_block_forward",
-    "qkv_heads_of_shard",
+    "qkv_heads_of_shard", "stack_forward",
 ]
 
 # ----------------------------------------------------------------------------
@@ -321,3 +327,30 @@ def sharded_block_forward(x, w: dict, n_heads: int, act: str, causal: bool, tp: 
         A_sh.append(a_b)
         U_sh.append(u_b)
     return Y, A_sh, U_sh
+
+
+def stack_forward(x, layers: list, n_heads: int, act: str, causal: bool, kcaches=None, vcaches=None,
+                  cache_pos: int = 0, act_dtype: str = "bf16", storage=None):
+    """A stack of blocks ([DMAP]: the layers of a model, each consuming the
+    previous one's output), every layer tensor-parallel as in block_forward.
+
+    ``layers`` holds one weight dict per layer; ``kcaches``/``vcaches`` one
+    cache per layer (or None).  The activation handed to layer l + 1 is
+    layer l's Y stored in ``act_dtype`` ("bf16": rounded to bf16; "fp32":
+    rounded to fp32).  Returns (last layer's Y, [K_new per layer],
+    [V_new per layer]).
+    """
+    h = to64(x)
+    Ks, Vs = [], []
+    for i, w in enumerate(layers):
+        kw = {}
+        if kcaches is not None:
+            kw = dict(kcache=kcaches[i], vcache=vcaches[i], cache_pos=cache_pos)
+        y, k, v = block_forward(h, w, n_heads, act, causal, storage=storage, **kw)
+        Ks.append(k)
+        Vs.append(v)
+        if i + 1 < len(layers):
+            h = round_bf16(y) if act_dtype == "bf16" else round_fp32(y)
+        else:
+            h = y
+    return h, Ks, Vs

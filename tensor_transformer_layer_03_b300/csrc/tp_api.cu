@@ -73,12 +73,46 @@ Workspace workspace_layout(const tp_plan_s* p, int batch, int seq) {
 const char* ptr_at(const void* base, size_t off) { return static_cast<const char*>(base) + off; }
 char* ptr_at(void* base, size_t off) { return static_cast<char*>(base) + off; }
 
+// Block workspace plus the two plan-dtype activation buffers of a stack.
+size_t stack_workspace_bytes(const tp_plan_s* p, int batch, int seq) {
+    return workspace_layout(p, batch, seq).total + 2 * align_up((size_t)batch * seq * p->d * p->esize, 1024);
+}
+
 }  // namespace
+
+// The block S1..S5 on a validated workspace layout; out_act (nullable)
+// receives a plan-dtype copy of Y (the next layer's input in a stack).
+static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int seq, int causal, void* k_cache,
+                                    void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
+                                    const Workspace& w, void* out_f32, void* out_act, void* stream);
 
 tp_status tpk::status_from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return TP_OK;
     strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
     return TP_ERR_CUDA;
+}
+
+static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int seq, int causal, void* k_cache,
+                                    void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
+                                    const Workspace& w, void* out_f32, void* out_act, void* stream) {
+    const int M = batch * seq;
+    void* qkv = ptr_at(workspace, w.qkv);
+    void* attn = ptr_at(workspace, w.attn);
+    void* hf32 = ptr_at(workspace, w.hf32);
+    void* hact = ptr_at(workspace, w.hact);
+    void* u = ptr_at(workspace, w.u);
+    void* gs = w.total > w.gemm ? ptr_at(workspace, w.gemm) : nullptr;
+    const size_t gsb = w.total - w.gemm;
+    tp_status s = tp_column_linear(p, TP_QKV, x, M, packed, qkv, gs, gsb, stream);
+    if (s != TP_OK) return s;
+    s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
+                           ptr_at(workspace, w.scratch), w.gemm - w.scratch, stream);
+    if (s != TP_OK) return s;
+    s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
+    if (s != TP_OK) return s;
+    s = tp_column_linear(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, stream);
+    if (s != TP_OK) return s;
+    return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, out_act, gs, gsb, stream);
 }
 
 extern "C" {
@@ -356,24 +390,45 @@ tp_status tp_block_forward(tp_plan_t p, const void* x, int batch, int seq, int c
     if (misaligned(workspace)) return TP_ERR_ALIGNMENT;
     const Workspace w = workspace_layout(p, batch, seq);
     if (ws_bytes < w.total) return TP_ERR_WORKSPACE_TOO_SMALL;
-    const int M = batch * seq;
-    void* qkv = ptr_at(workspace, w.qkv);
-    void* attn = ptr_at(workspace, w.attn);
-    void* hf32 = ptr_at(workspace, w.hf32);
-    void* hact = ptr_at(workspace, w.hact);
-    void* u = ptr_at(workspace, w.u);
-    void* gs = w.total > w.gemm ? ptr_at(workspace, w.gemm) : nullptr;
-    const size_t gsb = w.total - w.gemm;
-    tp_status s = tp_column_linear(p, TP_QKV, x, M, packed, qkv, gs, gsb, stream);
-    if (s != TP_OK) return s;
-    s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
-                           ptr_at(workspace, w.scratch), w.gemm - w.scratch, stream);
-    if (s != TP_OK) return s;
-    s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
-    if (s != TP_OK) return s;
-    s = tp_column_linear(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, stream);
-    if (s != TP_OK) return s;
-    return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, nullptr, gs, gsb, stream);
+    return block_forward_impl(p, x, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, packed, workspace,
+                              w, out_f32, nullptr, stream);
+}
+
+tp_status tp_stack_workspace_bytes(tp_plan_t p, int batch, int seq, size_t* bytes) {
+    if (!p || !bytes) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
+    *bytes = stack_workspace_bytes(p, batch, seq);
+    return TP_OK;
+}
+
+tp_status tp_stack_forward(tp_plan_t p, int n_layers, const void* const* packed_layers, const void* x, int batch,
+                           int seq, int causal, void* const* k_caches, void* const* v_caches, int cache_cap,
+                           int cache_pos, void* workspace, size_t ws_bytes, void* out_f32, void* stream) {
+    if (!p || !packed_layers || !x || !workspace || !out_f32) return TP_ERR_NULL_ARG;
+    if (n_layers <= 0 || batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
+    if ((k_caches == nullptr) != (v_caches == nullptr)) return TP_ERR_NULL_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        if (!packed_layers[l]) return TP_ERR_NULL_ARG;
+        if (misaligned(packed_layers[l])) return TP_ERR_ALIGNMENT;
+        if (k_caches && (!k_caches[l] || !v_caches[l])) return TP_ERR_NULL_ARG;
+    }
+    if (misaligned(workspace) || misaligned(x) || misaligned(out_f32)) return TP_ERR_ALIGNMENT;
+    if (ws_bytes < stack_workspace_bytes(p, batch, seq)) return TP_ERR_WORKSPACE_TOO_SMALL;
+    const Workspace w = workspace_layout(p, batch, seq);
+    // two plan-dtype activation buffers after the block workspace: layer l
+    // writes its output's copy into act[l % 2], layer l + 1 reads it
+    const size_t act_bytes = align_up((size_t)batch * seq * p->d * p->esize, 1024);
+    void* act[2] = {ptr_at(workspace, w.total), ptr_at(workspace, w.total + act_bytes)};
+    for (int l = 0; l < n_layers; ++l) {
+        const void* in = l == 0 ? x : act[(l - 1) % 2];
+        void* copy = l + 1 < n_layers ? act[l % 2] : nullptr;
+        const tp_status s =
+            block_forward_impl(p, in, batch, seq, causal, k_caches ? k_caches[l] : nullptr,
+                               v_caches ? v_caches[l] : nullptr, cache_cap, cache_pos, packed_layers[l], workspace, w,
+                               out_f32, copy, stream);
+        if (s != TP_OK) return s;
+    }
+    return TP_OK;
 }
 
 tp_status tp_sync_status(void* stream) {

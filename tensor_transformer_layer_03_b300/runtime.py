@@ -48,3 +48,36 @@ class TPBlock:
         self.plan.block_forward(x, B, T, causal, self.packed, self.workspace, out, k_cache, v_cache, cap, cache_pos,
                                 stream)
         return out
+
+
+class TPStack:
+    """n_layers blocks of one shape, each with its own weights on ``device``,
+    run through tp_stack_forward (the plan-dtype activation of layer l is the
+    input of layer l + 1)."""
+
+    def __init__(self, shape, tp_degree: int, dtype: str, layer_weights: list, device="cuda",
+                 max_batch: int = 1, max_seq: int = 1):
+        self.blocks = [TPBlock(shape, tp_degree, dtype, w, device=device, max_batch=1, max_seq=1)
+                       for w in layer_weights]
+        self.plan = self.blocks[0].plan
+        self.device = torch.device(device)
+        self.workspace = None
+        self.reserve(max_batch, max_seq)
+
+    def reserve(self, batch: int, seq: int):
+        ws = self.plan.stack_workspace_bytes(batch, seq)
+        if self.workspace is None or self.workspace.numel() < ws:
+            self.workspace = _dev_bytes(ws, self.device)
+
+    def forward(self, x: torch.Tensor, causal: bool, out: torch.Tensor | None = None, k_caches=None, v_caches=None,
+                cache_pos: int = 0, stream=None) -> torch.Tensor:
+        """x: device [B, T, d] in the plan dtype.  Returns the last layer's Y
+        fp32 [B, T, d].  k_caches / v_caches: one cache per layer, or None."""
+        B, T, d = x.shape
+        self.reserve(B, T)
+        if out is None:
+            out = torch.empty(B, T, d, dtype=torch.float32, device=self.device)
+        cap = 0 if k_caches is None else k_caches[0].shape[2]
+        self.plan.stack_forward([b.packed for b in self.blocks], x, B, T, causal, self.workspace, out, k_caches,
+                                v_caches, cap, cache_pos, stream)
+        return out

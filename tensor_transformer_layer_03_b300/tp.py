@@ -51,6 +51,9 @@ EXPORTS = {
     "tp_attention_heads": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p]),
     "tp_block_forward": (_i, [_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p, _p]),
     "tp_attention_decode_noalloc": (_i, [_p, _p, _i, _p, _p, _i, _i, _p, _p]),
+    "tp_stack_workspace_bytes": (_i, [_p, _i, _i, ctypes.POINTER(_sz)]),
+    "tp_stack_forward": (_i, [_p, _i, ctypes.POINTER(_p), _p, _i, _i, _i, ctypes.POINTER(_p), ctypes.POINTER(_p),
+                              _i, _i, _p, _sz, _p, _p]),
     "tp_sync_status": (_i, [_p]),
 }
 for _name, (_res, _args) in EXPORTS.items():
@@ -166,6 +169,20 @@ class Plan:
     def attention_decode_noalloc(self, qkv, batch, k_cache, v_cache, cache_cap, cache_pos, out, stream=None):
         check(tp_attention_decode_noalloc(self.handle, _ptr(qkv), batch, _ptr(k_cache), _ptr(v_cache), cache_cap,
                                           cache_pos, _ptr(out), _stream(stream)), "tp_attention_decode_noalloc")
+
+    def stack_workspace_bytes(self, batch, seq):
+        b = _sz()
+        check(tp_stack_workspace_bytes(self.handle, batch, seq, ctypes.byref(b)), "tp_stack_workspace_bytes")
+        return b.value
+
+    def stack_forward(self, packed_layers, x, batch, seq, causal, workspace, out_f32, k_caches=None, v_caches=None,
+                      cache_cap=0, cache_pos=0, stream=None):
+        n = len(packed_layers)
+        arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts]) if ts is not None else None
+        nbytes = workspace.numel() * workspace.element_size()
+        check(tp_stack_forward(self.handle, n, arr(packed_layers), _ptr(x), batch, seq, int(causal), arr(k_caches),
+                               arr(v_caches), cache_cap, cache_pos, _ptr(workspace), nbytes, _ptr(out_f32),
+                               _stream(stream)), "tp_stack_forward")
 
     def sync_status(self, stream=None):
         check(tp_sync_status(_stream(stream)), "tp_sync_status")

@@ -318,6 +318,55 @@ def pin_decode_equals_prefill(o):
     assert np.max(np.abs(Vd[:, :, 0] - V[:, :, T - 1])) < 1e-12
 
 
+def pin_stack_brute_force(o):
+    """A 3-layer stack equals brute force applied layer by layer with the
+    inter-layer activation rounded to bf16 by torch's cast ([DMAP]: each
+    layer consumes the previous one's output)."""
+    def rnd_rows(rows):
+        return torch.tensor(rows, dtype=torch.float64).to(torch.bfloat16).double().tolist()
+    rng = _rng(41)
+    B, T, d, H, f, L = 2, 4, 8, 2, 12, 3
+    layers = [_weights(rng, d, f, "swiglu") for _ in range(L)]
+    x = rng.standard_normal((B, T, d))
+    Y, Ks, _ = o.stack_forward(x, layers, H, "swiglu", True)
+    for b in range(B):
+        h = x[b].tolist()
+        for i, w in enumerate(layers):
+            h = bf_block_seq(h, _tolist(w), H, "swiglu", True)
+            if i + 1 < L:
+                h = rnd_rows(h)
+        assert np.max(np.abs(Y[b] - np.array(h))) < 1e-12
+    assert len(Ks) == L
+
+
+def pin_stack_closed_forms(o):
+    """One layer is the block; layers with zero output projections pass the
+    input through (rounded to the inter-layer dtype after every layer but the
+    last); a cached 2-layer stack's last decode row equals its prefill."""
+    rng = _rng(42)
+    B, T, d, H, f = 2, 5, 8, 2, 6
+    w = _weights(rng, d, f, "swiglu")
+    x = rng.standard_normal((B, T, d))
+    Y1, _, _ = o.stack_forward(x, [w], H, "swiglu", True)
+    Yb, _, _ = o.block_forward(x, w, H, "swiglu", True)
+    assert np.max(np.abs(Y1 - Yb)) == 0.0
+    w0 = dict(w, Wo=np.zeros((d, d)), Wd=np.zeros((d, f)))
+    Y3, _, _ = o.stack_forward(x, [w0, w0, w0], H, "swiglu", True)
+    assert np.max(np.abs(Y3 - o.round_bf16(x))) == 0.0
+    Y3f, _, _ = o.stack_forward(x, [w0, w0, w0], H, "swiglu", True, act_dtype="fp32")
+    assert np.max(np.abs(Y3f - o.round_fp32(x))) == 0.0
+    layers = [_weights(rng, d, f, "swiglu") for _ in range(2)]
+    Yp, K, V = o.stack_forward(x, layers, H, "swiglu", True)
+    cap, dh = 8, d // H
+    kcs = [np.zeros((B, H, cap, dh)) for _ in range(2)]
+    vcs = [np.zeros((B, H, cap, dh)) for _ in range(2)]
+    for i in range(2):
+        kcs[i][:, :, :T - 1] = K[i][:, :, :T - 1]
+        vcs[i][:, :, :T - 1] = V[i][:, :, :T - 1]
+    Yd, _, _ = o.stack_forward(x[:, T - 1:], layers, H, "swiglu", True, kcs, vcs, T - 1)
+    assert np.max(np.abs(Yd[:, 0] - Yp[:, T - 1])) < 1e-12
+
+
 def pin_round_bf16(o):
     # ties to even at 1: 1 + 2^-8 -> 1, 1 + 3*2^-8 -> 1 + 2^-6
     vals = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3.0, 0.0, 1e-30])

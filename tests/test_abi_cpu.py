@@ -147,6 +147,21 @@ def test_argument_validation_before_launch(tp):
     assert B(h, good, 1, 4, 1, None, None, 0, 0, good, good, 64, good, None) == 8  # workspace too small
     assert B(h, good, 1, 4, 1, None, None, 0, 0, good, None, 1 << 30, good, None) == 1
     assert B(h, good, 1, 0, 1, None, None, 0, 0, good, good, 1 << 30, good, None) == 2
+    # stack
+    S = tp.tp_stack_forward
+    arr = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    bad = (ctypes.c_void_p * 2)(0x10000, 0)
+    odd2 = (ctypes.c_void_p * 2)(0x10000, 0x20008)
+    assert S(h, 0, arr, good, 1, 4, 1, None, None, 0, 0, good, 1 << 30, good, None) == 2
+    assert S(h, 2, None, good, 1, 4, 1, None, None, 0, 0, good, 1 << 30, good, None) == 1
+    assert S(h, 2, bad, good, 1, 4, 1, None, None, 0, 0, good, 1 << 30, good, None) == 1
+    assert S(h, 2, odd2, good, 1, 4, 1, None, None, 0, 0, good, 1 << 30, good, None) == 7
+    assert S(h, 2, arr, good, 1, 4, 1, arr, None, 8, 0, good, 1 << 30, good, None) == 1   # one-sided caches
+    assert S(h, 2, arr, good, 1, 4, 1, None, None, 0, 0, good, 64, good, None) == 8       # workspace too small
+    sb = ctypes.c_size_t()
+    assert tp.tp_stack_workspace_bytes(h, 1, 4, ctypes.byref(sb)) == 0
+    ws = ctypes.c_size_t()
+    assert tp.tp_plan_sizes(h, 1, 4, None, ctypes.byref(ws)) == 0 and sb.value > ws.value
     # shard weights: SwiGLU needs Wup
     assert tp.tp_shard_weights(h, good, good, good, good, good, None, good, good, None) == 1
     tp.tp_plan_destroy(h)

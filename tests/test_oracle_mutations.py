@@ -11,7 +11,7 @@ from pins import ALL_PINS
 real = {n: getattr(o, n) for n in ("attention_head", "linear", "silu", "gelu_erf", "all_reduce_sum",
                                    "block_forward", "round_bf16", "check_plan", "multi_head_attention",
                                    "softmax_rows", "row_parallel_partials", "column_parallel_linear",
-                                   "sharded_block_forward")}
+                                   "sharded_block_forward", "stack_forward")}
 
 
 def _att_scale_dh(q, k, v, causal, q_pos0=0):
@@ -98,7 +98,27 @@ def _col_wrong(x, W, tp):
     return [o.linear(x, W[s::tp][:n]) for s in range(tp)]
 
 
+def _stack_no_rounding(x, layers, *a, **kw):
+    kw["act_dtype"] = "fp64"  # the inter-layer activation never stored in the plan dtype
+    return _stack_fp64(x, layers, *a, **kw)
+
+
+def _stack_fp64(x, layers, n_heads, act, causal, kcaches=None, vcaches=None, cache_pos=0, act_dtype="bf16",
+                storage=None):
+    h = o.to64(x)
+    for i, w in enumerate(layers):
+        kw = {} if kcaches is None else dict(kcache=kcaches[i], vcache=vcaches[i], cache_pos=cache_pos)
+        h, _, _ = o.block_forward(h, w, n_heads, act, causal, storage=storage, **kw)
+    return h, [], []
+
+
+def _stack_first_weights(x, layers, *a, **kw):
+    return real["stack_forward"](x, [layers[0]] * len(layers), *a, **kw)
+
+
 MUTATIONS = {
+    "stack skips the inter-layer storage rounding": ("stack_forward", _stack_no_rounding),
+    "stack reuses the first layer's weights": ("stack_forward", _stack_first_weights),
     "attention scale 1/d": ("attention_head", _att_scale_dh),
     "causal mask off by one": ("attention_head", _att_mask_shift),
     "causal mask dropped": ("attention_head", _att_no_mask),
