@@ -47,7 +47,14 @@ design notes):
   bf16 data path stores between steps: Q/K/V, the attention output, the bf16
   operand copy of H and U; H itself is kept in fp32 for the residual;
 * in a stack of layers the activation passed from one layer to the next is
-  stored in the plan dtype (``act_dtype``), in both storage modes.
+  stored in the plan dtype (``act_dtype``), in both storage modes;
+* the LLaMA-style variant (``llama_block_forward``; norms and rotary
+  position embedding are not on the pages) is pre-norm: H = X +
+  Attn(RMSNorm(X; g_attn)), Y = H + FFN(RMSNorm(H; g_ffn)), RMSNorm(x; g) =
+  x / sqrt(mean(x^2) + eps) * g; RoPE rotates each head's dimension pairs
+  (2i, 2i+1) of Q and K by the angle p * theta^(-2i/d_head) at absolute
+  position p (the pairing of the original rotary-embedding formulation);
+  the KV cache holds the rotated keys.
 
 Arrays may be numpy arrays or torch CPU tensors of any float dtype; every
 function returns float64 numpy arrays.
@@ -64,7 +71,7 @@ __all__ = [
     "linear", "gelu_erf", "silu", "softmax_rows", "attention_head",
     "multi_head_attention", "column_parallel_linear", "row_parallel_partials",
     "all_reduce_sum", "ffn", "block_forward", "sharded_block_forward",
-    "qkv_heads_of_shard", "stack_forward",
+    "qkv_heads_of_shard", "stack_forward", "rms_norm", "rope", "llama_block_forward",
 ]
 
 # ----------------------------------------------------------------------------
@@ -354,3 +361,72 @@ def stack_forward(x, layers: list, n_heads: int, act: str, causal: bool, kcaches
         else:
             h = y
     return h, Ks, Vs
+
+
+# ----------------------------------------------------------------------------
+# LLaMA-style pre-norm block (a reading: norms and RoPE are not on the pages)
+# ----------------------------------------------------------------------------
+
+def rms_norm(x, g, eps: float) -> np.ndarray:
+    """x / sqrt(mean over the last axis of x^2 + eps) * g."""
+    x, g = to64(x), to64(g)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * g
+
+
+def rope(x, positions, n_heads: int, theta: float) -> np.ndarray:
+    """Rotary position embedding of x [T, n_heads * d_head]: in every head,
+    the pair (2i, 2i+1) of token t is rotated by positions[t] * theta^(-2i/d_head)."""
+    x = to64(x).copy()
+    T, d = x.shape
+    dh = d // n_heads
+    i = np.arange(dh // 2)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta ** (-2.0 * i / dh)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    for h in range(n_heads):
+        ev = x[:, h * dh:(h + 1) * dh:2].copy()
+        od = x[:, h * dh + 1:(h + 1) * dh:2].copy()
+        x[:, h * dh:(h + 1) * dh:2] = ev * c - od * s
+        x[:, h * dh + 1:(h + 1) * dh:2] = ev * s + od * c
+    return x
+
+
+def llama_block_forward(x, w: dict, n_heads: int, causal: bool, eps: float, theta: float,
+                        kcache=None, vcache=None, cache_pos: int = 0, storage=None):
+    """Pre-norm block with RMSNorm (w["g_attn"], w["g_ffn"]) and RoPE (theta
+    <= 0: none), SwiGLU FFN, tensor-parallel linears as in block_forward.
+
+    x [B, T, d]; the T tokens sit at positions cache_pos..cache_pos+T-1.  The
+    norm's 1/rms is taken from the unrounded input; ``storage="bf16"`` rounds
+    the same points as block_forward (the normed operand of the FFN is the
+    rounded H times that scale).  Returns (Y, K_new (rotated), V_new).
+    """
+    x = to64(x)
+    B, T, d = x.shape
+    dh = d // n_heads
+    Y = np.empty((B, T, d))
+    Kn = np.empty((B, n_heads, T, dh))
+    Vn = np.empty((B, n_heads, T, dh))
+    pos = cache_pos + np.arange(T)
+    for b in range(B):
+        xb = x[b]
+        xn = rms_norm(xb, w["g_attn"], eps)
+        q, k, v = linear(xn, w["Wq"]), linear(xn, w["Wk"]), linear(xn, w["Wv"])
+        if theta > 0:
+            q, k = rope(q, pos, n_heads, theta), rope(k, pos, n_heads, theta)
+        q, k, v = _store(q, storage), _store(k, storage), _store(v, storage)
+        Kn[b] = k.reshape(T, n_heads, dh).transpose(1, 0, 2)
+        Vn[b] = v.reshape(T, n_heads, dh).transpose(1, 0, 2)
+        if kcache is not None:
+            kc = to64(kcache[b])[:, :cache_pos]
+            vc = to64(vcache[b])[:, :cache_pos]
+            kfull = np.concatenate([kc.transpose(1, 0, 2).reshape(cache_pos, d), k], axis=0)
+            vfull = np.concatenate([vc.transpose(1, 0, 2).reshape(cache_pos, d), v], axis=0)
+            a = multi_head_attention(q, kfull, vfull, n_heads, causal, q_pos0=cache_pos)
+        else:
+            a = multi_head_attention(q, k, v, n_heads, causal)
+        h = xb + linear(_store(a, storage), w["Wo"])
+        h_res = h if storage is None else round_fp32(h)
+        scale = 1.0 / np.sqrt(np.mean(h_res * h_res, axis=-1, keepdims=True) + eps)
+        hn = _store(h, storage) * scale * to64(w["g_ffn"])
+        Y[b] = h_res + ffn(hn, w, "swiglu", storage)
+    return Y, Kn, Vn

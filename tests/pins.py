@@ -100,6 +100,65 @@ def bf_block_seq(x, w, H, act, causal, kc=None, vc=None, P=0, rnd=None):
     return [[hres[t][c] + dn[t][c] for c in range(d)] for t in range(T)]
 
 
+def bf_llama_block_seq(x, w, H, causal, eps, theta, kc=None, vc=None, P=0):
+    """Pre-norm RMSNorm + RoPE block on one sequence with explicit loops:
+    every pair (2i, 2i+1) of a head rotated with math.cos / math.sin."""
+    T, d = len(x), len(x[0])
+    dh = d // H
+
+    def norm(rows, g):
+        out = []
+        for row in rows:
+            ms = sum(v * v for v in row) / len(row)
+            out.append([row[c] / math.sqrt(ms + eps) * g[c] for c in range(len(row))])
+        return out
+
+    def rot(rows):
+        if theta <= 0:
+            return rows
+        out = []
+        for t, row in enumerate(rows):
+            p = P + t
+            r2 = list(row)
+            for h in range(H):
+                for i in range(dh // 2):
+                    a, b = row[h * dh + 2 * i], row[h * dh + 2 * i + 1]
+                    ang = p * theta ** (-2.0 * i / dh)
+                    r2[h * dh + 2 * i] = a * math.cos(ang) - b * math.sin(ang)
+                    r2[h * dh + 2 * i + 1] = a * math.sin(ang) + b * math.cos(ang)
+            out.append(r2)
+        return out
+
+    xn = norm(x, w["g_attn"])
+    q = rot(bf_matvec_rows(xn, w["Wq"]))
+    k = rot(bf_matvec_rows(xn, w["Wk"]))
+    v_ = bf_matvec_rows(xn, w["Wv"])
+    keys, vals = [], []
+    for p in range(P):
+        keys.append([kc[h][p][c] for h in range(H) for c in range(dh)])
+        vals.append([vc[h][p][c] for h in range(H) for c in range(dh)])
+    keys += k
+    vals += v_
+    a = [[0.0] * d for _ in range(T)]
+    for h in range(H):
+        for i in range(T):
+            js = [j for j in range(len(keys)) if (not causal or j <= P + i)]
+            sc = [sum(q[i][h * dh + c] * keys[j][h * dh + c] for c in range(dh)) / math.sqrt(dh) for j in js]
+            m = max(sc)
+            e = [math.exp(t - m) for t in sc]
+            z = sum(e)
+            for c in range(dh):
+                a[i][h * dh + c] = sum(e[n] * vals[js[n]][h * dh + c] for n in range(len(js))) / z
+    o_ = bf_matvec_rows(a, w["Wo"])
+    hres = [[x[t][c] + o_[t][c] for c in range(d)] for t in range(T)]
+    hn = norm(hres, w["g_ffn"])
+    g = bf_matvec_rows(hn, w["Wg"])
+    u_ = bf_matvec_rows(hn, w["Wu"])
+    u = [[bf_silu(g[t][n]) * u_[t][n] for n in range(len(g[0]))] for t in range(T)]
+    dn = bf_matvec_rows(u, w["Wd"])
+    return [[hres[t][c] + dn[t][c] for c in range(d)] for t in range(T)]
+
+
 def _tolist(w):
     return {n: a.tolist() for n, a in w.items()}
 
@@ -365,6 +424,84 @@ def pin_stack_closed_forms(o):
         vcs[i][:, :, :T - 1] = V[i][:, :, :T - 1]
     Yd, _, _ = o.stack_forward(x[:, T - 1:], layers, H, "swiglu", True, kcs, vcs, T - 1)
     assert np.max(np.abs(Yd[:, 0] - Yp[:, T - 1])) < 1e-12
+
+
+def _llama_weights(rng, d, f):
+    w = _weights(rng, d, f, "swiglu")
+    w["g_attn"] = 1.0 + 0.5 * rng.standard_normal(d)
+    w["g_ffn"] = 1.0 + 0.5 * rng.standard_normal(d)
+    return w
+
+
+def pin_llama_brute_force(o):
+    """The pre-norm RMSNorm + RoPE block against explicit loops, with and
+    without a cache (positions offset by the cache length) and without RoPE."""
+    for causal, theta, P in ((True, 10000.0, 0), (False, 10000.0, 0), (True, 500.0, 3), (True, 0.0, 0)):
+        rng = _rng(51 + P + int(theta) % 7)
+        B, T, d, H, f, cap = 2, 4, 8, 2, 6, 7
+        w = _llama_weights(rng, d, f)
+        x = rng.standard_normal((B, T, d))
+        kc = rng.standard_normal((B, H, cap, d // H))
+        vc = rng.standard_normal((B, H, cap, d // H))
+        kw = dict(kcache=kc, vcache=vc, cache_pos=P) if P else {}
+        Y, _, _ = o.llama_block_forward(x, w, H, causal, 1e-5, theta, **kw)
+        wl = {n: a.tolist() for n, a in w.items()}
+        for b in range(B):
+            ref = np.array(bf_llama_block_seq(x[b].tolist(), wl, H, causal, 1e-5, theta,
+                                              kc[b].tolist() if P else None, vc[b].tolist() if P else None, P))
+            assert np.max(np.abs(Y[b] - ref)) < 1e-11, (causal, theta, P)
+
+
+def pin_rope_properties(o):
+    """RoPE equals multiplying each pair, read as a complex number, by
+    exp(i p theta^(-2i/dh)); it keeps every pair's norm; position 0 is the
+    identity; q at m and k at n score the same as q at m+s and k at n+s."""
+    rng = _rng(52)
+    T, H, dh, theta = 6, 3, 8, 10000.0
+    x = rng.standard_normal((T, H * dh))
+    pos = np.array([0, 1, 5, 17, 100, 2047])
+    r = o.rope(x, pos, H, theta)
+    z = x.reshape(T, H, dh // 2, 2)
+    zc = z[..., 0] + 1j * z[..., 1]
+    rot = np.exp(1j * pos[:, None, None] * theta ** (-2.0 * np.arange(dh // 2) / dh)[None, None, :])
+    ref = zc * rot
+    got = r.reshape(T, H, dh // 2, 2)
+    assert np.max(np.abs(got[..., 0] - ref.real)) < 1e-12 and np.max(np.abs(got[..., 1] - ref.imag)) < 1e-12
+    assert np.max(np.abs(np.abs(got[..., 0] + 1j * got[..., 1]) - np.abs(zc))) < 1e-12
+    assert np.max(np.abs(r[0] - x[0])) == 0.0
+    q, k = rng.standard_normal((1, dh)), rng.standard_normal((1, dh))
+    for m, n, sh in ((3, 1, 7), (10, 10, 100), (0, 5, 33)):
+        a = o.rope(q, [m], 1, theta) @ o.rope(k, [n], 1, theta).T
+        b = o.rope(q, [m + sh], 1, theta) @ o.rope(k, [n + sh], 1, theta).T
+        assert abs(float((a - b).item())) < 1e-10
+
+
+def pin_rms_norm(o):
+    """torch's float64 rms_norm; scale invariance; a constant row c maps to
+    sign(c) * g (eps = 0)."""
+    rng = _rng(53)
+    x = rng.standard_normal((5, 16))
+    g = rng.standard_normal(16)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (16,), torch.from_numpy(g), eps=1e-6).numpy()
+    assert np.max(np.abs(o.rms_norm(x, g, 1e-6) - ref)) < 1e-12
+    assert np.max(np.abs(o.rms_norm(3.7 * x, g, 0.0) - o.rms_norm(x, g, 0.0))) < 1e-12
+    c = np.full((2, 16), -2.5)
+    assert np.max(np.abs(o.rms_norm(c, g, 0.0) - (-g))) < 1e-12
+
+
+def pin_llama_decode_equals_prefill(o):
+    """The last token decoded over the cache of the earlier tokens' rotated
+    K/V equals the prefill's last row."""
+    rng = _rng(54)
+    B, T, d, H, f = 2, 6, 16, 4, 8
+    w = _llama_weights(rng, d, f)
+    x = rng.standard_normal((B, T, d))
+    Y, K, V = o.llama_block_forward(x, w, H, True, 1e-5, 10000.0)
+    kc, vc = np.zeros((B, H, 8, d // H)), np.zeros((B, H, 8, d // H))
+    kc[:, :, :T - 1], vc[:, :, :T - 1] = K[:, :, :T - 1], V[:, :, :T - 1]
+    Yd, Kd, _ = o.llama_block_forward(x[:, T - 1:], w, H, True, 1e-5, 10000.0, kc, vc, T - 1)
+    assert np.max(np.abs(Yd[:, 0] - Y[:, T - 1])) < 1e-12
+    assert np.max(np.abs(Kd[:, :, 0] - K[:, :, T - 1])) < 1e-12
 
 
 def pin_round_bf16(o):

@@ -11,7 +11,7 @@ from pins import ALL_PINS
 real = {n: getattr(o, n) for n in ("attention_head", "linear", "silu", "gelu_erf", "all_reduce_sum",
                                    "block_forward", "round_bf16", "check_plan", "multi_head_attention",
                                    "softmax_rows", "row_parallel_partials", "column_parallel_linear",
-                                   "sharded_block_forward", "stack_forward")}
+                                   "sharded_block_forward", "stack_forward", "rope", "rms_norm")}
 
 
 def _att_scale_dh(q, k, v, causal, q_pos0=0):
@@ -116,7 +116,40 @@ def _stack_first_weights(x, layers, *a, **kw):
     return real["stack_forward"](x, [layers[0]] * len(layers), *a, **kw)
 
 
+def _rope_half(x, positions, n_heads, theta):
+    # pairs (i, i + dh/2) instead of (2i, 2i+1)
+    x = o.to64(x).copy()
+    T, d = x.shape
+    dh = d // n_heads
+    i = np.arange(dh // 2)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta ** (-2.0 * i / dh)[None, :]
+    c, s_ = np.cos(ang), np.sin(ang)
+    for h in range(n_heads):
+        a = x[:, h * dh:h * dh + dh // 2].copy()
+        b = x[:, h * dh + dh // 2:(h + 1) * dh].copy()
+        x[:, h * dh:h * dh + dh // 2] = a * c - b * s_
+        x[:, h * dh + dh // 2:(h + 1) * dh] = a * s_ + b * c
+    return x
+
+
+def _rope_neg(x, positions, n_heads, theta):
+    return real["rope"](x, -np.asarray(positions), n_heads, theta)
+
+
+def _rms_no_eps(x, g, eps):
+    return real["rms_norm"](x, g, 0.0)
+
+
+def _rms_mean_abs(x, g, eps):
+    x, g = o.to64(x), o.to64(g)
+    return x / (np.mean(np.abs(x), axis=-1, keepdims=True) + eps) * g
+
+
 MUTATIONS = {
+    "rope pairs (i, i + d/2)": ("rope", _rope_half),
+    "rope angle sign": ("rope", _rope_neg),
+    "rms norm without eps": ("rms_norm", _rms_no_eps),
+    "rms norm by mean |x|": ("rms_norm", _rms_mean_abs),
     "stack skips the inter-layer storage rounding": ("stack_forward", _stack_no_rounding),
     "stack reuses the first layer's weights": ("stack_forward", _stack_first_weights),
     "attention scale 1/d": ("attention_head", _att_scale_dh),
