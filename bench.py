@@ -207,12 +207,13 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def bench_decode(args, dev, flush=None, batch=1, timeline=False):
+def bench_decode(args, dev, flush=None, batch=1, timeline=False, prenorm=False):
     """One-token decode step of the 7B-shaped block (tp 2, 1024 cached
     positions + the new one) for `batch` sequences, captured in a CUDA graph;
     HBM GB/s against the algorithmic bytes (every packed weight once + the
     K/V cache read).  With `timeline`, also the device start/end of every
-    kernel of one replay (CUPTI through torch.profiler)."""
+    kernel of one replay (CUPTI through torch.profiler).  `prenorm`: the
+    RMSNorm + RoPE variant of the block (two more launches per step)."""
     import torch
 
     from tensor_transformer_layer_03_b300 import inputs as I
@@ -223,7 +224,12 @@ def bench_decode(args, dev, flush=None, batch=1, timeline=False):
     s = wl.shape
     B, P = wl.batch, wl.cache_len
     cap = P + 1
-    blk = TPBlock(s, wl.tp, wl.dtype, w, device=dev, max_batch=B, max_seq=1)
+    norm = {}
+    if prenorm:
+        w.update(I.make_norm_gains(s, wl.dtype, torch.Generator().manual_seed(1)))
+        norm = {"rms_eps": 1e-5, "rope_theta": 10000.0}
+    n_launch = 8 if prenorm else 6
+    blk = TPBlock(s, wl.tp, wl.dtype, w, device=dev, max_batch=B, max_seq=1, **norm)
     kc = torch.zeros(B, s.n_heads, cap, s.d_head, dtype=torch.bfloat16, device=dev)
     vc = torch.zeros_like(kc)
     kc[:, :, :P] = inp["Kcache"].to(dev)
@@ -259,7 +265,7 @@ def bench_decode(args, dev, flush=None, batch=1, timeline=False):
                     graph.replay()
                 st.synchronize()
             ks = sorted((e.time_range.start, e.time_range.end, e.name) for e in prof.events()
-                        if e.device_type.name == "CUDA")[-6:]
+                        if e.device_type.name == "CUDA")[-n_launch:]
             t0 = ks[0][0]
             tl = [{"kernel": n.replace("(anonymous namespace)::", "").replace("void ", "").split("(")[0],
                    "start_us": round(a - t0, 2), "end_us": round(b - t0, 2)} for a, b, n in ks]
@@ -272,10 +278,10 @@ def bench_decode(args, dev, flush=None, batch=1, timeline=False):
     med = statistics.median(us)
     gbs = algo / (med * 1e-6) / 1e9
     pk = peaks()
-    return {"workload": "llama7b_decode", "tp_degree": wl.tp, "batch": B, "cache_positions": P + 1,
+    return {"workload": "llama7b_decode" + ("_prenorm" if prenorm else ""), "tp_degree": wl.tp, "batch": B, "cache_positions": P + 1,
             "us_per_step_median": med, "us_per_step_p10": sorted(us)[len(us) // 10],
             "algorithmic_bytes": algo, "gb_s": gbs, "hbm_peak_gb_s": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
-            "tokens_per_s": B / (med * 1e-6), "graph": True, "launches_per_step": 6,
+            "tokens_per_s": B / (med * 1e-6), "graph": True, "launches_per_step": n_launch,
             "l2": f"not flushed: each step streams {algo / 1e6:.1f} MB of weights and cache (> 126 MB L2)",
             **({"timeline": tl} if tl else {})}
 
@@ -293,16 +299,23 @@ def run_sweep(args):
     pk = peaks()
     wls = I.sweep_workloads() + [I.WORKLOADS["llama13b_b4t1024"].with_(name=f"llama13b_b4t1024_tp{t}", tp=t)
                                  for t in I.TP_SWEEP]
+    # the pre-norm (RMSNorm + RoPE) variant of the 7B prefill block
+    wls.append(I.WORKLOADS["llama7b_prefill"].with_(name="llama7b_prefill_prenorm"))
     st = torch.cuda.Stream(device=dev)
     blk, key = None, None
     for wl in wls:
         gen = torch.Generator().manual_seed(0)
-        if key != (wl.shape, wl.tp):  # one set of packed weights per block shape and degree
+        pre = wl.name.endswith("_prenorm")
+        if key != (wl.shape, wl.tp, pre):  # one set of packed weights per block variant and degree
             blk = None
             torch.cuda.empty_cache()
             w = I.make_weights(wl.shape, wl.dtype, gen)
-            blk = TPBlock(wl.shape, wl.tp, wl.dtype, w, device=dev)
-            key = (wl.shape, wl.tp)
+            norm = {}
+            if pre:
+                w.update(I.make_norm_gains(wl.shape, wl.dtype, gen))
+                norm = {"rms_eps": 1e-5, "rope_theta": 10000.0}
+            blk = TPBlock(wl.shape, wl.tp, wl.dtype, w, device=dev, **norm)
+            key = (wl.shape, wl.tp, pre)
             del w
         blk.reserve(wl.batch, wl.seq)
         x = torch.randn(wl.batch, wl.seq, wl.shape.d_model, generator=gen).to(torch.bfloat16).to(dev)
@@ -358,8 +371,10 @@ def run_sweep(args):
     # batched one-token decode at 1024 cached positions (7B shape, tp 2)
     for b in (1, 4, 16, 64):
         r = bench_decode(args, dev, batch=b)
-        print(json.dumps({"workload": f"llama7b_decode_b{b}", **r}), flush=True)
+        print(json.dumps({**r, "workload": f"llama7b_decode_b{b}"}), flush=True)
         torch.cuda.empty_cache()
+    r = bench_decode(args, dev, batch=1, prenorm=True)
+    print(json.dumps({**r, "workload": "llama7b_decode_prenorm_b1"}), flush=True)
     return 0
 
 

@@ -265,6 +265,37 @@ tp_status tp_stack_forward(tp_plan_t plan, int n_layers, const void* const* pack
                            void* stream);
 
 /*
+ * Pre-norm (LLaMA-style) variant of the block.  Norms and rotary embedding
+ * are not on the pages ("What Is Tensor Parallelism?", netray.co, and
+ * undercodenews.com/?p=110319 shard only the linears and attention); this
+ * is the usual reading of a LLaMA-shaped block, with the same
+ * tensor-parallel split:
+ *   H = X + Attn(RMSNorm(X; g_attn)),  Y = H + SwiGLU-FFN(RMSNorm(H; g_ffn)),
+ *   RMSNorm(x; g) = x / sqrt(mean(x^2) + rms_eps) * g,
+ * and Q, K rotated per head: the pair (2i, 2i+1) of the token at absolute
+ * position p (cache_pos + t) by the angle p * rope_theta^(-2i/d_head)
+ * (rope_theta 0: no rotation).  The KV cache holds rotated keys.
+ *
+ * tp_plan_create_llama: bf16, SwiGLU; rms_eps > 0 and finite, rope_theta
+ *   >= 0 and finite (else TP_ERR_INVALID_DIM); the tp_plan_create_ex rules;
+ *   d_ffn/tp a multiple of 32 (else TP_ERR_UNSUPPORTED).
+ * tp_shard_weights_llama: as tp_shard_weights, then the gains g_attn,
+ *   g_ffn (device, bf16 [d_model], 16-byte aligned) are multiplied into the
+ *   packed QKV and gate/up columns (W diag(g), rounded to bf16), so the
+ *   norm costs one fp32 row scale in the linears' epilogues.
+ *   TP_ERR_UNSUPPORTED on a plan not made by tp_plan_create_llama.
+ * tp_block_forward / tp_stack_forward take such a plan unchanged (the
+ *   workspace sizes include the per-row scales); tp_column_linear returns
+ *   TP_ERR_UNSUPPORTED for it (its inputs lack the norm scales and
+ *   positions); tp_row_linear_reduce and tp_attention_heads are unchanged.
+ */
+tp_status tp_plan_create_llama(int d_model, int n_heads, int d_ffn, int tp_degree, float rms_eps,
+                               float rope_theta, tp_plan_t* out);
+tp_status tp_shard_weights_llama(tp_plan_t plan, const void* Wq, const void* Wk, const void* Wv,
+                                 const void* Wo, const void* Wgate, const void* Wup, const void* Wdown,
+                                 const void* g_attn, const void* g_ffn, void* packed, void* stream);
+
+/*
  * Wait for `stream`, then report (and clear) the first device-side error
  * recorded by a bounded wait in this library's kernels on the current
  * device: TP_ERR_DEVICE_TIMEOUT, TP_ERR_CUDA on a CUDA error, else TP_OK.

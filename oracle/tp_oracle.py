@@ -398,9 +398,20 @@ def llama_block_forward(x, w: dict, n_heads: int, causal: bool, eps: float, thet
     x [B, T, d]; the T tokens sit at positions cache_pos..cache_pos+T-1.  The
     norm's 1/rms is taken from the unrounded input; ``storage="bf16"`` rounds
     the same points as block_forward (the normed operand of the FFN is the
-    rounded H times that scale).  Returns (Y, K_new (rotated), V_new).
+    rounded H times that scale) and stores each gain folded into the weight
+    columns that read the normed rows: W diag(g), rounded once, with the gain
+    then 1 (equal to the unfolded form in exact arithmetic).  Returns
+    (Y, K_new (rotated), V_new).
     """
     x = to64(x)
+    if storage is not None:
+        w = dict(w)
+        ga, gf = to64(w["g_attn"]), to64(w["g_ffn"])
+        for k in ("Wq", "Wk", "Wv"):
+            w[k] = _store(to64(w[k]) * ga[None, :], storage)
+        for k in ("Wg", "Wu"):
+            w[k] = _store(to64(w[k]) * gf[None, :], storage)
+        w["g_attn"], w["g_ffn"] = np.ones_like(ga), np.ones_like(gf)
     B, T, d = x.shape
     dh = d // n_heads
     Y = np.empty((B, T, d))

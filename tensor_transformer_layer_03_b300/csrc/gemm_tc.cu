@@ -82,7 +82,31 @@ struct Params {
     // splitk_reduce_k sums them in split order and applies the epilogue
     int splits;
     float* partials;
+    // pre-norm variant: see TcGemm
+    const float* row_scale;
+    int rope_cols, rope_dh, rope_seq, rope_pos0;
+    float rope_log2_theta;
 };
+
+// Rotary position embedding of `n` (even) consecutive values of one row
+// starting at column `col` (even) of a shard: pairs (2i, 2i+1) of each head
+// of width p.rope_dh rotated by pos * theta^(-2i/dh); only columns below
+// p.rope_cols (the shard's Q and K heads) are rotated.
+template <int N>
+__device__ __forceinline__ void apply_rope(const Params& p, int row, int col, float (&v)[N]) {
+    if (col >= p.rope_cols) return;
+    const float pos = (float)(p.rope_pos0 + row % p.rope_seq);
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) {
+        const int i = ((col + 2 * j) % p.rope_dh) / 2;
+        const float ang = pos * exp2f(-(float)(2 * i) / (float)p.rope_dh * p.rope_log2_theta);
+        float sn, cs;
+        sincosf(ang, &sn, &cs);
+        const float a = v[2 * j], b = v[2 * j + 1];
+        v[2 * j] = a * cs - b * sn;
+        v[2 * j + 1] = a * sn + b * cs;
+    }
+}
 
 using namespace ptx;
 
@@ -357,8 +381,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld32(tbase + 64 * g + 32, up);
                     const int pc = col_base + 64 * g;  // packed column of this gate block
                     if (row_ok && pc < p.N) {
+                        const float rs = p.row_scale ? p.row_scale[row] : 1.f;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) gate[j] = silu(gate[j]) * up[j];
+                        for (int j = 0; j < 32; ++j) gate[j] = silu(gate[j] * rs) * (up[j] * rs);
                         store_row_bf16(out + pc / 2, gate, 32);
                     }
                 }
@@ -431,6 +456,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld32(tbase + 32 * c, v);
                     const int col = col_base + 32 * c;
                     if (!row_ok || col >= p.N) continue;
+                    if (p.row_scale) {
+                        const float rs = p.row_scale[row];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= rs;
+                    }
+                    if (p.rope_cols > 0) apply_rope<32>(p, row, col, v);
                     if (p.epi == EPI_GELU) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
@@ -488,10 +519,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_k(Params p) {
                 ga.x += gb.x; ga.y += gb.y; ga.z += gb.z; ga.w += gb.w;
                 ua.x += ub.x; ua.y += ub.y; ua.z += ub.z; ua.w += ub.w;
             }
-            v[0] = silu(ga.x) * ua.x;
-            v[1] = silu(ga.y) * ua.y;
-            v[2] = silu(ga.z) * ua.z;
-            v[3] = silu(ga.w) * ua.w;
+            const float sc = p.row_scale ? p.row_scale[row] : 1.f;
+            v[0] = silu(ga.x * sc) * (ua.x * sc);
+            v[1] = silu(ga.y * sc) * (ua.y * sc);
+            v[2] = silu(ga.z * sc) * (ua.z * sc);
+            v[3] = silu(ga.w * sc) * (ua.w * sc);
         } else {
             float4 a = __ldcg(reinterpret_cast<const float4*>(base + col));
             for (int sp = 1; sp < p.splits; ++sp) {
@@ -502,6 +534,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_k(Params p) {
             v[1] = a.y;
             v[2] = a.z;
             v[3] = a.w;
+            if (p.row_scale) {
+                const float sc = p.row_scale[row];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] *= sc;
+            }
+            if (p.rope_cols > 0) apply_rope<4>(p, row, col, v);
             if (p.epi == EPI_GELU) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] = gelu_erf(v[j]);
@@ -659,6 +697,12 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     p.granule = g.granule;
     p.err = dev_err;
     p.timeout_ns = DEFAULT_TIMEOUT_NS;
+    p.row_scale = g.row_scale;
+    p.rope_cols = g.rope_cols;
+    p.rope_dh = g.rope_dh;
+    p.rope_seq = g.rope_seq > 0 ? g.rope_seq : 1;
+    p.rope_pos0 = g.rope_pos0;
+    p.rope_log2_theta = g.rope_log2_theta;
     p.splits = 1;
     // split-K when whole tiles would leave at least half of the units idle
     if (scratch && 2 * p.n_tiles <= slots) {

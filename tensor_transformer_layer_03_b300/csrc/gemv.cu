@@ -149,9 +149,41 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
             row_dots2<MT>(W + gate_row * g.K, X, W + (gate_row + g.granule) * g.K, X, g.lda, g.K, ag, au);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const float gs = warp_sum(ag[m]), us = warp_sum(au[m]);
+                const float rs = g.row_scale ? g.row_scale[m] : 1.f;  // pre-norm: 1/rms of input row m
+                const float gs = warp_sum(ag[m]) * rs, us = warp_sum(au[m]) * rs;
                 if (lane == 0)
                     ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + j] = __float2bfloat16_rn(silu(gs) * us);
+            }
+        }
+    } else if (g.rope_cols > 0) {
+        // rotary embedding rotates output pairs (2i, 2i+1): a warp takes the
+        // adjacent items 2k, 2k+1 (N is even, so a pair never straddles shards)
+        const int pairs = g.shards * g.N / 2;
+        for (int k = gw; k < pairs; k += nw) {
+            const int it = 2 * k;
+            float acc[2][MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
+            row_dots2<MT>(W + (long long)it * g.K, X, W + (long long)(it + 1) * g.K, X, g.lda, g.K, acc[0], acc[1]);
+            const int s = it / g.N, n = it % g.N;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float rs = g.row_scale ? g.row_scale[m] : 1.f;
+                float a = warp_sum(acc[0][m]) * rs, b = warp_sum(acc[1][m]) * rs;
+                if (n < g.rope_cols) {
+                    const int i = (n % g.rope_dh) / 2;
+                    const float pos = (float)(g.rope_pos0 + m % (g.rope_seq > 0 ? g.rope_seq : 1));
+                    float sn, cs;
+                    sincosf(pos * exp2f(-(float)(2 * i) / (float)g.rope_dh * g.rope_log2_theta), &sn, &cs);
+                    const float a2 = a * cs - b * sn;
+                    b = a * sn + b * cs;
+                    a = a2;
+                }
+                if (lane == 0) {
+                    bf16* o = (bf16*)g.out + s * g.out_shard + (long long)m * g.ldo + n;
+                    o[0] = __float2bfloat16_rn(a);
+                    o[1] = __float2bfloat16_rn(b);
+                }
             }
         }
     } else {
@@ -174,6 +206,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     float v = warp_sum(acc[r][m]);
+                    if (g.row_scale) v *= g.row_scale[m];
                     if (EPI == EPI_GELU) v = gelu_erf(v);
                     if (lane == 0) ((bf16*)g.out)[s * g.out_shard + (long long)m * g.ldo + n] = __float2bfloat16_rn(v);
                 }

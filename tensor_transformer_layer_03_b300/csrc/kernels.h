@@ -74,6 +74,15 @@ struct TcGemm {
     void* out2;
     const void* residual;
     int residual_f32;
+    // pre-norm variant (column-parallel launches only): the accumulator row
+    // m is scaled by row_scale[m] (1/rms of input row m; the norm's gain is
+    // folded into W), and for rope_cols > 0 the first rope_cols columns of
+    // every shard (its Q and K heads) get rotary position embedding: pair
+    // (2i, 2i+1) of a head of width rope_dh rotated by
+    // pos * 2^(-(2i/rope_dh) * rope_log2_theta), pos = rope_pos0 + m % rope_seq
+    const float* row_scale;
+    int rope_cols, rope_dh, rope_seq, rope_pos0;
+    float rope_log2_theta;
 };
 bool tc_gemm_supported(int M, int N, int K);
 // scratch (nullable): stream-K partials and flags, at least
@@ -86,6 +95,13 @@ typedef TcGemm GemvArgs;
 constexpr int GEMV_MAX_M = 8;
 bool gemv_supported(const GemvArgs& g);
 cudaError_t gemv(const GemvArgs& g, int* dev_err, cudaStream_t st);
+
+// ---- pre-norm helpers (norm.cu) ----------------------------------------------
+// W[r][c] *= gamma[c] for rows x d (plan dtype, rounded back to it).
+cudaError_t scale_cols(int esize, void* W, long long rows, int d, const void* gamma, cudaStream_t st);
+// r[m] = 1 / sqrt(mean_c x[m][c]^2 + eps), x bf16 (x_f32 = 0) or fp32,
+// d a multiple of 8 and rows 16-byte aligned.
+cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, cudaStream_t st);
 
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
 bool tc_attention_supported(const AttnArgs& a);

@@ -12,6 +12,10 @@ struct tp_plan_s {
     tp_act act;
     tp_dtype dtype;
     int esize;
+    // pre-norm variant (tp_plan_create_llama): RMSNorm before attention and
+    // FFN, rotary embedding of Q and K (rope_theta 0: none)
+    int llama;
+    float eps, rope_theta;
     size_t off_qkv, off_o, off_up, off_down, packed_bytes;
 };
 

@@ -3,6 +3,7 @@
 // Everything here runs on the host.  Calls validate their arguments before
 // enqueuing anything, then launch the kernels of pack.cu, simt.cu,
 // gemm_tc.cu, attn_tc.cu and decode.cu on the caller's stream.
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -40,7 +41,7 @@ int* device_error_word() {
 }
 
 struct Workspace {
-    size_t qkv, attn, hf32, hact, u, scratch, gemm, total;
+    size_t qkv, attn, hf32, hact, u, scratch, gemm, rs, total;
 };
 
 // Stream-K scratch of the tensor-core GEMMs (bf16 plans, M past the
@@ -66,6 +67,7 @@ Workspace workspace_layout(const tp_plan_s* p, int batch, int seq) {
     w.u = o;     o = align_up(o + (size_t)p->tp * M * p->fl * es, 1024);
     w.scratch = o; o = align_up(o + attn_scratch_bytes(p, batch, seq), 1024);
     w.gemm = o;    o = align_up(o + linear_scratch_bytes(p, (long long)batch * seq), 1024);
+    w.rs = o;      o = align_up(o + (p->llama ? 2 * M * sizeof(float) : 0), 1024);  // 1/rms of x and of H
     w.total = o;
     return w;
 }
@@ -86,6 +88,17 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
                                     void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
                                     const Workspace& w, void* out_f32, void* out_act, void* stream);
 
+// Pre-norm extras of a column-parallel launch: row scales (1/rms of the
+// input rows) and the rotary embedding of the QKV output.
+struct ColumnExtras {
+    const float* row_scale = nullptr;
+    int rope = 0, rope_seq = 1, rope_pos0 = 0;
+};
+
+static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M, const void* packed,
+                                    void* out_shards, void* scratch, size_t scratch_bytes, const ColumnExtras& ex,
+                                    cudaStream_t st);
+
 tp_status tpk::status_from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return TP_OK;
     strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
@@ -101,16 +114,35 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     void* hf32 = ptr_at(workspace, w.hf32);
     void* hact = ptr_at(workspace, w.hact);
     void* u = ptr_at(workspace, w.u);
-    void* gs = w.total > w.gemm ? ptr_at(workspace, w.gemm) : nullptr;
-    const size_t gsb = w.total - w.gemm;
-    tp_status s = tp_column_linear(p, TP_QKV, x, M, packed, qkv, gs, gsb, stream);
+    void* gs = w.rs > w.gemm ? ptr_at(workspace, w.gemm) : nullptr;
+    const size_t gsb = w.rs - w.gemm;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* r1 = reinterpret_cast<float*>(ptr_at(workspace, w.rs));
+    float* r2 = r1 + M;
+    ColumnExtras ex1, ex2;
+    if (p->llama) {
+        // RMSNorm of x (its gain is in the packed QKV rows), RoPE at the
+        // tokens' positions cache_pos + t inside the QKV epilogue
+        cudaError_t e = tpk::rms_rows(x, p->dtype == TP_FP32, M, p->d, p->eps, r1, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        ex1.row_scale = r1;
+        ex1.rope = p->rope_theta > 0.f;
+        ex1.rope_seq = seq;
+        ex1.rope_pos0 = cache_pos;
+        ex2.row_scale = r2;
+    }
+    tp_status s = column_linear_impl(p, TP_QKV, x, M, packed, qkv, gs, gsb, ex1, st);
     if (s != TP_OK) return s;
     s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
                            ptr_at(workspace, w.scratch), w.gemm - w.scratch, stream);
     if (s != TP_OK) return s;
     s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
     if (s != TP_OK) return s;
-    s = tp_column_linear(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, stream);
+    if (p->llama) {  // RMSNorm of H: scale from the fp32 H, the GEMM reads its plan-dtype copy
+        cudaError_t e = tpk::rms_rows(hf32, 1, M, p->d, p->eps, r2, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    s = column_linear_impl(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, ex2, st);
     if (s != TP_OK) return s;
     return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, out_act, gs, gsb, stream);
 }
@@ -166,6 +198,9 @@ tp_status tp_plan_create_ex(int d_model, int n_heads, int d_ffn, int tp_degree, 
     p->dtype = dtype;
     p->esize = dtype == TP_BF16 ? 2 : 4;
     p->up_rows = act == TP_ACT_SWIGLU ? 2 * fl : fl;
+    p->llama = 0;
+    p->eps = 0.f;
+    p->rope_theta = 0.f;
     const size_t es = p->esize, d = d_model, T = tp_degree;
     size_t o = 0;
     p->off_qkv = o;  o = align_up(o + T * 3 * p->hl * dh * d * es, 1024);
@@ -179,6 +214,26 @@ tp_status tp_plan_create_ex(int d_model, int n_heads, int d_ffn, int tp_degree, 
 
 tp_status tp_plan_create(int d_model, int n_heads, int d_ffn, int tp_degree, tp_plan_t* out) {
     return tp_plan_create_ex(d_model, n_heads, d_ffn, tp_degree, TP_ACT_SWIGLU, TP_BF16, out);
+}
+
+tp_status tp_plan_create_llama(int d_model, int n_heads, int d_ffn, int tp_degree, float rms_eps, float rope_theta,
+                               tp_plan_t* out) {
+    if (!out) return TP_ERR_NULL_ARG;
+    *out = nullptr;
+    if (!(rms_eps > 0.f) || !isfinite(rms_eps) || !(rope_theta >= 0.f) || !isfinite(rope_theta))
+        return TP_ERR_INVALID_DIM;
+    const tp_status s = tp_plan_create_ex(d_model, n_heads, d_ffn, tp_degree, TP_ACT_SWIGLU, TP_BF16, out);
+    if (s != TP_OK) return s;
+    tp_plan_s* p = *out;
+    if (p->granule != 32) {  // the tensor-core SwiGLU epilogue pairs 32-row gate/up blocks
+        delete p;
+        *out = nullptr;
+        return TP_ERR_UNSUPPORTED;
+    }
+    p->llama = 1;
+    p->eps = rms_eps;
+    p->rope_theta = rope_theta;
+    return TP_OK;
 }
 
 void tp_plan_destroy(tp_plan_t plan) { delete plan; }
@@ -223,13 +278,42 @@ tp_status tp_shard_weights(tp_plan_t p, const void* Wq, const void* Wk, const vo
     return cuda_status(e);
 }
 
+tp_status tp_shard_weights_llama(tp_plan_t p, const void* Wq, const void* Wk, const void* Wv, const void* Wo,
+                                 const void* Wgate, const void* Wup, const void* Wdown, const void* g_attn,
+                                 const void* g_ffn, void* packed, void* stream) {
+    if (!p || !g_attn || !g_ffn) return TP_ERR_NULL_ARG;
+    if (!p->llama) return TP_ERR_UNSUPPORTED;
+    if (misaligned(g_attn) || misaligned(g_ffn)) return TP_ERR_ALIGNMENT;
+    const tp_status s = tp_shard_weights(p, Wq, Wk, Wv, Wo, Wgate, Wup, Wdown, packed, stream);
+    if (s != TP_OK) return s;
+    // fold the norms' gains into the columns of the rows that read the
+    // normed activations: all QKV rows and all gate/up rows
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = tpk::scale_cols(p->esize, ptr_at(packed, p->off_qkv), (long long)p->tp * 3 * p->hl * p->dh,
+                                    p->d, g_attn, st);
+    if (e == cudaSuccess)
+        e = tpk::scale_cols(p->esize, ptr_at(packed, p->off_up), (long long)p->tp * p->up_rows, p->d, g_ffn, st);
+    return cuda_status(e);
+}
+
 tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const void* packed, void* out_shards,
                            void* scratch, size_t scratch_bytes, void* stream) {
     if (!p || !x || !packed || !out_shards) return TP_ERR_NULL_ARG;
     if (M <= 0 || (which != TP_QKV && which != TP_FFN_UP)) return TP_ERR_INVALID_DIM;
     if (misaligned(x) || misaligned(packed) || misaligned(out_shards) || misaligned(scratch))
         return TP_ERR_ALIGNMENT;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // a pre-norm plan's column linears need the norm scales and positions
+    // that only the whole-block calls compute
+    if (p->llama) return TP_ERR_UNSUPPORTED;
+    return column_linear_impl(p, which, x, M, packed, out_shards, scratch, scratch_bytes, ColumnExtras(),
+                              static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M, const void* packed,
+                                    void* out_shards, void* scratch, size_t scratch_bytes, const ColumnExtras& ex,
+                                    cudaStream_t st) {
     const bool qkv = which == TP_QKV;
     const int N = qkv ? 3 * p->hl * p->dh : p->up_rows;  // W rows per shard
     const int n_out = qkv ? N : p->fl;                     // output columns per shard
@@ -252,10 +336,19 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
         g.out_shard = (long long)M * n_out;
         g.ldo = n_out;
         g.granule = p->granule;
+        g.row_scale = ex.row_scale;
+        if (ex.rope) {
+            g.rope_cols = 2 * p->hl * p->dh;  // the Q and K heads of each shard's [Q | K | V] row
+            g.rope_dh = p->dh;
+            g.rope_seq = ex.rope_seq;
+            g.rope_pos0 = ex.rope_pos0;
+            g.rope_log2_theta = log2f(p->rope_theta);
+        }
         if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, device_error_word(), st));
         if (tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32))
             return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
+    if (ex.row_scale) return TP_ERR_UNSUPPORTED;  // (plan creation rules this out for pre-norm plans)
     tpk::SimtGemm g{};
     g.epi = epi;
     g.is_bf16 = p->dtype == TP_BF16;
@@ -276,6 +369,8 @@ tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const v
     g.granule = p->granule;
     return cuda_status(tpk::simt_gemm(g, st));
 }
+
+extern "C" {
 
 tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
                                const void* residual, void* out_f32, void* out_act, void* scratch,

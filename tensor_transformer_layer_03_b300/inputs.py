@@ -108,6 +108,15 @@ def make_weights(shape: BlockShape, dtype: str, gen: torch.Generator) -> dict:
     return out
 
 
+def make_norm_gains(shape: BlockShape, dtype: str, gen: torch.Generator) -> dict:
+    """RMSNorm gains of the pre-norm block variant: g_attn, g_ffn [d_model],
+    1 + N(0, 0.25^2) (a trained model's gains sit near 1)."""
+    dt = torch_dtype(dtype)
+    d = shape.d_model
+    return {"g_attn": (1.0 + 0.25 * torch.randn(d, generator=gen)).to(dt),
+            "g_ffn": (1.0 + 0.25 * torch.randn(d, generator=gen)).to(dt)}
+
+
 def make_inputs(wl: Workload, seed: int = 0) -> dict:
     """All tensors of one workload, on the CPU, in the workload's dtype."""
     gen = torch.Generator().manual_seed(seed)

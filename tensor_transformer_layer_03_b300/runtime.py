@@ -17,12 +17,16 @@ def _dev_bytes(nbytes: int, device) -> torch.Tensor:
 
 
 class TPBlock:
-    """One tensor-parallel block with its weights resident on ``device``."""
+    """One tensor-parallel block with its weights resident on ``device``.
+
+    rms_eps given: the pre-norm variant (RMSNorm with the gains
+    weights["g_attn"], weights["g_ffn"], rotary embedding with rope_theta)."""
 
     def __init__(self, shape, tp_degree: int, dtype: str, weights: dict, device="cuda",
-                 max_batch: int = 1, max_seq: int = 1, stream=None):
+                 max_batch: int = 1, max_seq: int = 1, stream=None, rms_eps=None, rope_theta: float = 0.0):
         self.shape, self.tp, self.dtype, self.device = shape, tp_degree, dtype, torch.device(device)
-        self.plan = _tp.Plan(shape.d_model, shape.n_heads, shape.d_ffn, tp_degree, act=shape.act, dtype=dtype)
+        self.plan = _tp.Plan(shape.d_model, shape.n_heads, shape.d_ffn, tp_degree, act=shape.act, dtype=dtype,
+                             rms_eps=rms_eps, rope_theta=rope_theta)
         packed_bytes, _ = self.plan.sizes(1, 1)
         self.packed = _dev_bytes(packed_bytes, self.device)
         dev_w = {k: v.to(self.device, non_blocking=False).contiguous() for k, v in weights.items()}
@@ -56,8 +60,9 @@ class TPStack:
     input of layer l + 1)."""
 
     def __init__(self, shape, tp_degree: int, dtype: str, layer_weights: list, device="cuda",
-                 max_batch: int = 1, max_seq: int = 1):
-        self.blocks = [TPBlock(shape, tp_degree, dtype, w, device=device, max_batch=1, max_seq=1)
+                 max_batch: int = 1, max_seq: int = 1, rms_eps=None, rope_theta: float = 0.0):
+        self.blocks = [TPBlock(shape, tp_degree, dtype, w, device=device, max_batch=1, max_seq=1, rms_eps=rms_eps,
+                               rope_theta=rope_theta)
                        for w in layer_weights]
         self.plan = self.blocks[0].plan
         self.device = torch.device(device)

@@ -41,10 +41,12 @@ EXPORTS = {
     "tp_last_cuda_error": (ctypes.c_char_p, []),
     "tp_plan_create": (_i, [_i, _i, _i, _i, _plan_p]),
     "tp_plan_create_ex": (_i, [_i, _i, _i, _i, _i, _i, _plan_p]),
+    "tp_plan_create_llama": (_i, [_i, _i, _i, _i, ctypes.c_float, ctypes.c_float, _plan_p]),
     "tp_plan_destroy": (None, [_p]),
     "tp_plan_sizes": (_i, [_p, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     "tp_attention_scratch_bytes": (_i, [_p, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tp_shard_weights": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "tp_shard_weights_llama": (_i, [_p] * 12),
     "tp_linear_scratch_bytes": (_i, [_p, _i, ctypes.POINTER(_sz)]),
     "tp_column_linear": (_i, [_p, _i, _p, _i, _p, _p, _p, _sz, _p]),
     "tp_row_linear_reduce": (_i, [_p, _i, _p, _i, _p, _p, _p, _p, _p, _sz, _p]),
@@ -100,12 +102,23 @@ def _stream(stream):
 class Plan:
     """Owns a tp_plan_t.  Methods take torch tensors (device pointers)."""
 
-    def __init__(self, d_model, n_heads, d_ffn, tp_degree, act="swiglu", dtype="bf16"):
+    def __init__(self, d_model, n_heads, d_ffn, tp_degree, act="swiglu", dtype="bf16", rms_eps=None,
+                 rope_theta=0.0):
+        """rms_eps given: the pre-norm (RMSNorm + RoPE) variant, which is
+        SwiGLU and bf16 only (tp_plan_create_llama)."""
         h = ctypes.c_void_p()
-        code = tp_plan_create_ex(d_model, n_heads, d_ffn, tp_degree,
-                                 TP_ACT_SWIGLU if act == "swiglu" else TP_ACT_GELU,
-                                 TP_BF16 if dtype == "bf16" else TP_FP32, ctypes.byref(h))
-        check(code, "tp_plan_create_ex")
+        self.llama = rms_eps is not None
+        if self.llama:
+            if act != "swiglu" or dtype != "bf16":
+                raise ValueError("the pre-norm block is SwiGLU and bf16")
+            code = tp_plan_create_llama(d_model, n_heads, d_ffn, tp_degree, float(rms_eps), float(rope_theta),
+                                        ctypes.byref(h))
+            check(code, "tp_plan_create_llama")
+        else:
+            code = tp_plan_create_ex(d_model, n_heads, d_ffn, tp_degree,
+                                     TP_ACT_SWIGLU if act == "swiglu" else TP_ACT_GELU,
+                                     TP_BF16 if dtype == "bf16" else TP_FP32, ctypes.byref(h))
+            check(code, "tp_plan_create_ex")
         self.handle = h
         self.d_model, self.n_heads, self.d_ffn, self.tp = d_model, n_heads, d_ffn, tp_degree
         self.d_head = d_model // n_heads
@@ -132,6 +145,11 @@ class Plan:
     def shard_weights(self, w: dict, packed, stream=None):
         up = w.get("Wu")
         first = w["Wg"] if up is not None else w["W1"]
+        if self.llama:
+            check(tp_shard_weights_llama(self.handle, _ptr(w["Wq"]), _ptr(w["Wk"]), _ptr(w["Wv"]), _ptr(w["Wo"]),
+                                         _ptr(first), _ptr(up), _ptr(w["Wd"]), _ptr(w["g_attn"]), _ptr(w["g_ffn"]),
+                                         _ptr(packed), _stream(stream)), "tp_shard_weights_llama")
+            return
         check(tp_shard_weights(self.handle, _ptr(w["Wq"]), _ptr(w["Wk"]), _ptr(w["Wv"]), _ptr(w["Wo"]),
                                _ptr(first), _ptr(up), _ptr(w["Wd"]), _ptr(packed), _stream(stream)),
               "tp_shard_weights")

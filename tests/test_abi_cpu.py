@@ -176,3 +176,42 @@ def test_unsupported_head_width(tp):
     good = ctypes.c_void_p(0x10000)
     assert tp.tp_attention_heads(h, good, 1, 4, 1, None, None, 0, 0, good, None, 0, None) == 9
     tp.tp_plan_destroy(h)
+
+
+def _create_llama(tp, d, H, f, deg, eps=1e-5, theta=10000.0):
+    h = ctypes.c_void_p()
+    code = tp.tp_plan_create_llama(d, H, f, deg, eps, theta, ctypes.byref(h))
+    return code, h
+
+
+def test_llama_plan_rules_and_validation(tp):
+    """The pre-norm plan: its own argument rules, the block rules of
+    tp_plan_create_ex, the 32-row FFN granule, and the calls it refuses."""
+    nan, inf = float("nan"), float("inf")
+    for eps, theta in ((0.0, 1e4), (-1e-5, 1e4), (nan, 1e4), (inf, 1e4), (1e-5, -1.0), (1e-5, nan), (1e-5, inf)):
+        code, h = _create_llama(tp, 256, 4, 1024, 2, eps, theta)
+        assert code == 2 and not h.value, (eps, theta)
+    assert tp.tp_plan_create_llama(256, 4, 1024, 2, 1e-5, 1e4, None) == 1
+    assert _create_llama(tp, 256, 4, 1024, 3)[0] == 4      # heads not divisible by the degree
+    assert _create_llama(tp, 256, 4, 1040, 2)[0] == 9      # d_ffn/tp = 520: no 32-row gate/up blocks
+    code, h0 = _create(tp, 256, 4, 1024, 2)
+    code, h = _create_llama(tp, 256, 4, 1024, 2, theta=0.0)  # theta 0: RMSNorm without rotation
+    assert code == 0 and h.value
+    good, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+    # column linears of a pre-norm plan need the norm scales: refused
+    assert tp.tp_column_linear(h, 0, good, 4, good, good, None, 0, None) == 9
+    assert tp.tp_column_linear(h, 1, good, 512, good, good, None, 0, None) == 9
+    SW = tp.tp_shard_weights_llama
+    args = [good] * 7
+    assert SW(h0, *args, good, good, good, None) == 9      # not a pre-norm plan
+    assert SW(h, *args, None, good, good, None) == 1
+    assert SW(h, *args, good, None, good, None) == 1
+    assert SW(h, *args, odd, good, good, None) == 7
+    assert SW(h, good, good, good, good, good, None, good, good, good, good, None) == 1  # SwiGLU needs Wup
+    # same packed weights, a workspace with room for the 1/rms rows
+    pw0, ws0, pw, ws = (ctypes.c_size_t() for _ in range(4))
+    assert tp.tp_plan_sizes(h0, 2, 64, ctypes.byref(pw0), ctypes.byref(ws0)) == 0
+    assert tp.tp_plan_sizes(h, 2, 64, ctypes.byref(pw), ctypes.byref(ws)) == 0
+    assert pw.value == pw0.value and ws.value >= ws0.value + 2 * 128 * 4
+    tp.tp_plan_destroy(h)
+    tp.tp_plan_destroy(h0)

@@ -1,0 +1,109 @@
+"""GPU parity of the pre-norm (RMSNorm + RoPE) block against the float64
+oracle's llama_block_forward: prefill on the tensor-core linears (whole
+tiles and split-K), with and without rotation, the 7B shape, multi-step
+decode with a growing cache on the weight-streaming and tensor-core linears,
+and a two-layer stack.  Bounds as in test_gpu_block.py: normwise <= 2e-2
+against the exact oracle, mean abs against the oracle's bf16-storage floor
+(which stores the gains folded into the bf16 weights, as the library does)."""
+import pytest
+import torch
+
+import oracle.tp_oracle as o
+from helpers import BF16_MEAN_ABS, FLOOR_FACTOR, assert_close_bf16, mean_abs
+from tensor_transformer_layer_03_b300 import inputs as I
+from tensor_transformer_layer_03_b300.runtime import TPBlock, TPStack
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+EPS = 1e-5
+
+
+def _weights(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    w = I.make_weights(shape, "bf16", g)
+    w.update(I.make_norm_gains(shape, "bf16", g))
+    return w, g
+
+
+def _check(got, ex, st, what):
+    floor = mean_abs(st, ex)
+    return assert_close_bf16(got, ex, what, mean_abs_bound=max(BF16_MEAN_ABS, FLOOR_FACTOR * floor))
+
+
+@pytest.mark.parametrize("shape,deg,B,T,theta", [
+    (I.BlockShape(512, 8, 1536, "swiglu"), 4, 2, 160, 10000.0),     # whole tiles, ragged tail
+    (I.BlockShape(1024, 8, 2816, "swiglu"), 2, 1, 300, 500000.0),   # split-K linears
+    (I.BlockShape(512, 4, 1536, "swiglu"), 2, 3, 129, 0.0),         # norms only, no rotation
+])
+def test_llama_prefill(tp, shape, deg, B, T, theta):
+    w, g = _weights(shape, 31)
+    x = torch.randn(B, T, shape.d_model, generator=g).to(torch.bfloat16)
+    blk = TPBlock(shape, deg, "bf16", w, device=DEV, max_batch=B, max_seq=T, rms_eps=EPS, rope_theta=theta)
+    y = blk.forward(x.to(DEV), True).cpu()
+    blk.plan.sync_status()
+    ex, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, theta)
+    st, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, theta, storage="bf16")
+    _check(y, ex, st, f"pre-norm prefill d={shape.d_model} theta={theta}")
+
+
+def test_llama7b_prefill(tp):
+    shape, B, T = I.LLAMA7B, 1, 256
+    w, g = _weights(shape, 32)
+    x = torch.randn(B, T, shape.d_model, generator=g).to(torch.bfloat16)
+    blk = TPBlock(shape, 2, "bf16", w, device=DEV, max_batch=B, max_seq=T, rms_eps=EPS, rope_theta=10000.0)
+    y = blk.forward(x.to(DEV), True).cpu()
+    blk.plan.sync_status()
+    ex, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, 10000.0)
+    st, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, 10000.0, storage="bf16")
+    _check(y, ex, st, "7B pre-norm prefill")
+
+
+@pytest.mark.parametrize("B,shape,deg,P,n", [
+    (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 5),    # weight-streaming linears (M <= 8)
+    (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 4),   # tensor-core linears
+])
+def test_llama_multistep_decode(tp, B, shape, deg, P, n):
+    """n single-token steps at positions P..P+n-1 equal one oracle pass of the
+    n tokens over the P-position prefix; the appended keys are rotated."""
+    w, g = _weights(shape, 33)
+    H, dh, theta = shape.n_heads, shape.d_head, 10000.0
+    x = torch.randn(B, n, shape.d_model, generator=g).to(torch.bfloat16)
+    cap = P + n + 3
+    kc = torch.full((B, H, cap, dh), float("nan"), dtype=torch.bfloat16)
+    vc = torch.full((B, H, cap, dh), float("nan"), dtype=torch.bfloat16)
+    kc[:, :, :P] = torch.randn(B, H, P, dh, generator=g).to(torch.bfloat16)
+    vc[:, :, :P] = torch.randn(B, H, P, dh, generator=g).to(torch.bfloat16)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    blk = TPBlock(shape, deg, "bf16", w, device=DEV, max_batch=B, max_seq=1, rms_eps=EPS, rope_theta=theta)
+    xd = x.to(DEV)
+    ys = [blk.forward(xd[:, i:i + 1].contiguous(), True, k_cache=kd, v_cache=vd, cache_pos=P + i).cpu()
+          for i in range(n)]
+    blk.plan.sync_status()
+    got = torch.cat(ys, dim=1)
+    ex, K, _ = o.llama_block_forward(x, w, H, True, EPS, theta, kcache=kc, vcache=vc, cache_pos=P)
+    st, _, _ = o.llama_block_forward(x, w, H, True, EPS, theta, kcache=kc, vcache=vc, cache_pos=P, storage="bf16")
+    _check(got, ex, st, f"pre-norm {n}-step decode B={B}")
+    kn = kd.cpu()
+    assert torch.isnan(kn[:, :, P + n:]).all(), "cache rows past the last step were written"
+    # keys are stored rotated: bf16 of the oracle's rotated K, within the
+    # bf16 path's bound
+    assert_close_bf16(kn[:, :, P:P + n], o.round_bf16(K), "appended rotated K rows")
+
+
+def test_llama_stack_prefill(tp):
+    """Two pre-norm layers; the layer input is the bf16 copy of the previous
+    layer's output (the stack's hand-off), composed here from two oracle
+    passes."""
+    shape, deg, B, T, theta = I.BlockShape(512, 8, 1536, "swiglu"), 2, 2, 96, 10000.0
+    w0, g = _weights(shape, 34)
+    w1, _ = _weights(shape, 35)
+    x = torch.randn(B, T, shape.d_model, generator=g).to(torch.bfloat16)
+    stk = TPStack(shape, deg, "bf16", [w0, w1], device=DEV, max_batch=B, max_seq=T, rms_eps=EPS, rope_theta=theta)
+    y = stk.forward(x.to(DEV), True).cpu()
+    stk.plan.sync_status()
+    outs = []
+    for storage in (None, "bf16"):
+        h, _, _ = o.llama_block_forward(x, w0, shape.n_heads, True, EPS, theta, storage=storage)
+        h, _, _ = o.llama_block_forward(o.round_bf16(h), w1, shape.n_heads, True, EPS, theta, storage=storage)
+        outs.append(h)
+    _check(y, outs[0], outs[1], "2-layer pre-norm stack")
