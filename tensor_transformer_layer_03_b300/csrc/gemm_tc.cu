@@ -84,27 +84,34 @@ struct Params {
     float* partials;
     // pre-norm variant: see TcGemm
     const float* row_scale;
-    int rope_cols, rope_dh, rope_seq, rope_pos0;
-    float rope_log2_theta;
+    int rope_cols, rope_dh, rope_seq;
+    const float2* rope_cs;
 };
 
-// Rotary position embedding of `n` (even) consecutive values of one row
-// starting at column `col` (even) of a shard: pairs (2i, 2i+1) of each head
-// of width p.rope_dh rotated by pos * theta^(-2i/dh); only columns below
-// p.rope_cols (the shard's Q and K heads) are rotated.
+// Rotary position embedding of N consecutive values of one row starting at
+// column `col` of a shard (col a multiple of N, N a multiple of 4): pairs
+// (2i, 2i+1) of each head of width p.rope_dh rotated by the table's angle
+// for the row's position; only columns below p.rope_cols (the shard's Q and
+// K heads; a multiple of 8) are rotated.  d_head is a multiple of 8, so 4
+// columns never straddle two heads or the Q/K-V boundary, and each float4
+// of the table holds their two pairs.
 template <int N>
 __device__ __forceinline__ void apply_rope(const Params& p, int row, int col, float (&v)[N]) {
     if (col >= p.rope_cols) return;
-    const float pos = (float)(p.rope_pos0 + row % p.rope_seq);
+    const int half = p.rope_dh / 2;
+    const float2* tr = p.rope_cs + (long long)(row % p.rope_seq) * half;
+    int hc = col % p.rope_dh;  // column within the head, advanced 4 at a time
 #pragma unroll
-    for (int j = 0; j < N / 2; ++j) {
-        const int i = ((col + 2 * j) % p.rope_dh) / 2;
-        const float ang = pos * exp2f(-(float)(2 * i) / (float)p.rope_dh * p.rope_log2_theta);
-        float sn, cs;
-        sincosf(ang, &sn, &cs);
-        const float a = v[2 * j], b = v[2 * j + 1];
-        v[2 * j] = a * cs - b * sn;
-        v[2 * j + 1] = a * sn + b * cs;
+    for (int q = 0; q < N / 4; ++q) {
+        if (col + 4 * q >= p.rope_cols) break;
+        const float4 c = *reinterpret_cast<const float4*>(tr + hc / 2);
+        const float a0 = v[4 * q], b0 = v[4 * q + 1], a1 = v[4 * q + 2], b1 = v[4 * q + 3];
+        v[4 * q] = a0 * c.x - b0 * c.y;
+        v[4 * q + 1] = a0 * c.y + b0 * c.x;
+        v[4 * q + 2] = a1 * c.z - b1 * c.w;
+        v[4 * q + 3] = a1 * c.w + b1 * c.z;
+        hc += 4;
+        if (hc >= p.rope_dh) hc -= p.rope_dh;
     }
 }
 
@@ -701,8 +708,7 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     p.rope_cols = g.rope_cols;
     p.rope_dh = g.rope_dh;
     p.rope_seq = g.rope_seq > 0 ? g.rope_seq : 1;
-    p.rope_pos0 = g.rope_pos0;
-    p.rope_log2_theta = g.rope_log2_theta;
+    p.rope_cs = g.rope_cs;
     p.splits = 1;
     // split-K when whole tiles would leave at least half of the units idle
     if (scratch && 2 * p.n_tiles <= slots) {

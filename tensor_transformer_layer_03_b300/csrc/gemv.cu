@@ -171,12 +171,11 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
                 const float rs = g.row_scale ? g.row_scale[m] : 1.f;
                 float a = warp_sum(acc[0][m]) * rs, b = warp_sum(acc[1][m]) * rs;
                 if (n < g.rope_cols) {
-                    const int i = (n % g.rope_dh) / 2;
-                    const float pos = (float)(g.rope_pos0 + m % (g.rope_seq > 0 ? g.rope_seq : 1));
-                    float sn, cs;
-                    sincosf(pos * exp2f(-(float)(2 * i) / (float)g.rope_dh * g.rope_log2_theta), &sn, &cs);
-                    const float a2 = a * cs - b * sn;
-                    b = a * sn + b * cs;
+                    const float2 c =
+                        g.rope_cs[(long long)(m % (g.rope_seq > 0 ? g.rope_seq : 1)) * (g.rope_dh / 2) +
+                                  (n % g.rope_dh) / 2];
+                    const float a2 = a * c.x - b * c.y;
+                    b = a * c.y + b * c.x;
                     a = a2;
                 }
                 if (lane == 0) {

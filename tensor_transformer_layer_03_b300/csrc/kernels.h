@@ -78,11 +78,11 @@ struct TcGemm {
     // m is scaled by row_scale[m] (1/rms of input row m; the norm's gain is
     // folded into W), and for rope_cols > 0 the first rope_cols columns of
     // every shard (its Q and K heads) get rotary position embedding: pair
-    // (2i, 2i+1) of a head of width rope_dh rotated by
-    // pos * 2^(-(2i/rope_dh) * rope_log2_theta), pos = rope_pos0 + m % rope_seq
+    // (2i, 2i+1) of a head of width rope_dh in row m rotated by the angle
+    // whose (cos, sin) is rope_cs[(m % rope_seq) * rope_dh / 2 + i]
     const float* row_scale;
-    int rope_cols, rope_dh, rope_seq, rope_pos0;
-    float rope_log2_theta;
+    int rope_cols, rope_dh, rope_seq;
+    const float2* rope_cs;
 };
 bool tc_gemm_supported(int M, int N, int K);
 // scratch (nullable): stream-K partials and flags, at least
@@ -99,9 +99,18 @@ cudaError_t gemv(const GemvArgs& g, int* dev_err, cudaStream_t st);
 // ---- pre-norm helpers (norm.cu) ----------------------------------------------
 // W[r][c] *= gamma[c] for rows x d (plan dtype, rounded back to it).
 cudaError_t scale_cols(int esize, void* W, long long rows, int d, const void* gamma, cudaStream_t st);
+// Rotary table: cs[t * half + i] = (cos, sin) of (pos0 + t) * 2^(-(2i / (2 half)) * log2_theta)
+// for t < seq, i < half (half = d_head / 2).
+struct RopeTable {
+    float2* cs;
+    int seq, pos0, half;
+    float log2_theta;
+};
 // r[m] = 1 / sqrt(mean_c x[m][c]^2 + eps), x bf16 (x_f32 = 0) or fp32,
-// d a multiple of 8 and rows 16-byte aligned.
-cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, cudaStream_t st);
+// d a multiple of 8 and rows 16-byte aligned; the same launch fills
+// rope->cs when rope is non-null.
+cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, const RopeTable* rope,
+                     cudaStream_t st);
 
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
 bool tc_attention_supported(const AttnArgs& a);

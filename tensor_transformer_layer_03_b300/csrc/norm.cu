@@ -39,14 +39,38 @@ __device__ __forceinline__ float sumsq8(const float* p) {
     return a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
 }
 
+// Launched with programmatic dependent launch: lets the next kernel start
+// at entry and waits for the previous one before reading x or writing.
+// Four chunks per lane are loaded before they are summed (memory-level
+// parallelism).  Blocks past the first rms_blocks fill the rotary table.
 template <typename E>
-__global__ void rms_rows_k(const E* __restrict__ x, int M, int d, float eps, float* __restrict__ r) {
+__global__ void rms_rows_k(const E* __restrict__ x, int M, int d, float eps, float* __restrict__ r, RopeTable rt,
+                           int rms_blocks) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if ((int)blockIdx.x >= rms_blocks) {
+        const int idx = ((int)blockIdx.x - rms_blocks) * blockDim.x + threadIdx.x;
+        if (idx < rt.seq * rt.half) {
+            const int t = idx / rt.half, i = idx % rt.half;
+            const float ang = (float)(rt.pos0 + t) * exp2f(-(float)(2 * i) / (float)(2 * rt.half) * rt.log2_theta);
+            float sn, cs;
+            sincosf(ang, &sn, &cs);
+            rt.cs[idx] = make_float2(cs, sn);
+        }
+        return;
+    }
     const int lane = threadIdx.x % 32;
     const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (row >= M) return;
     const E* xr = x + (long long)row * d;
     float s = 0.f;
-    for (int c = lane * 8; c < d; c += 256) s += sumsq8(xr + c);
+    int c = lane * 8;
+    for (; c + 3 * 256 < d; c += 4 * 256) {
+        const float a = sumsq8(xr + c), b = sumsq8(xr + c + 256), e = sumsq8(xr + c + 512),
+                    f = sumsq8(xr + c + 768);
+        s += (a + b) + (e + f);
+    }
+    for (; c < d; c += 256) s += sumsq8(xr + c);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) r[row] = rsqrtf(s / (float)d + eps);
@@ -65,13 +89,23 @@ cudaError_t scale_cols(int esize, void* W, long long rows, int d, const void* ga
     return cudaGetLastError();
 }
 
-cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, cudaStream_t st) {
-    const int blocks = (M + 7) / 8;
-    if (x_f32)
-        rms_rows_k<float><<<blocks, 256, 0, st>>>((const float*)x, M, d, eps, r);
-    else
-        rms_rows_k<bf16><<<blocks, 256, 0, st>>>((const bf16*)x, M, d, eps, r);
-    return cudaGetLastError();
+cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, const RopeTable* rope,
+                     cudaStream_t st) {
+    const int rms_blocks = (M + 7) / 8;
+    RopeTable rt = {};
+    if (rope) rt = *rope;
+    const long long entries = rope ? (long long)rt.seq * rt.half : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rms_blocks + (unsigned)((entries + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (x_f32) return cudaLaunchKernelEx(&cfg, rms_rows_k<float>, (const float*)x, M, d, eps, r, rt, rms_blocks);
+    return cudaLaunchKernelEx(&cfg, rms_rows_k<bf16>, (const bf16*)x, M, d, eps, r, rt, rms_blocks);
 }
 
 }  // namespace tpk

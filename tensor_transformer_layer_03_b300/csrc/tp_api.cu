@@ -41,7 +41,7 @@ int* device_error_word() {
 }
 
 struct Workspace {
-    size_t qkv, attn, hf32, hact, u, scratch, gemm, rs, total;
+    size_t qkv, attn, hf32, hact, u, scratch, gemm, rs, rope, total;
 };
 
 // Stream-K scratch of the tensor-core GEMMs (bf16 plans, M past the
@@ -68,6 +68,7 @@ Workspace workspace_layout(const tp_plan_s* p, int batch, int seq) {
     w.scratch = o; o = align_up(o + attn_scratch_bytes(p, batch, seq), 1024);
     w.gemm = o;    o = align_up(o + linear_scratch_bytes(p, (long long)batch * seq), 1024);
     w.rs = o;      o = align_up(o + (p->llama ? 2 * M * sizeof(float) : 0), 1024);  // 1/rms of x and of H
+    w.rope = o;    o = align_up(o + (p->llama ? (size_t)seq * (p->dh / 2) * sizeof(float2) : 0), 1024);
     w.total = o;
     return w;
 }
@@ -92,7 +93,8 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
 // input rows) and the rotary embedding of the QKV output.
 struct ColumnExtras {
     const float* row_scale = nullptr;
-    int rope = 0, rope_seq = 1, rope_pos0 = 0;
+    const float2* rope_cs = nullptr;  // rotary (cos, sin) table, NULL: no rotation
+    int rope_seq = 1;
 };
 
 static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M, const void* packed,
@@ -121,14 +123,21 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     float* r2 = r1 + M;
     ColumnExtras ex1, ex2;
     if (p->llama) {
-        // RMSNorm of x (its gain is in the packed QKV rows), RoPE at the
-        // tokens' positions cache_pos + t inside the QKV epilogue
-        cudaError_t e = tpk::rms_rows(x, p->dtype == TP_FP32, M, p->d, p->eps, r1, st);
+        // RMSNorm of x (its gain is in the packed QKV rows) and, in the same
+        // launch, the rotary table of positions cache_pos + t, applied in
+        // the QKV epilogue
+        tpk::RopeTable rt = {};
+        rt.cs = reinterpret_cast<float2*>(ptr_at(workspace, w.rope));
+        rt.seq = seq;
+        rt.pos0 = cache_pos;
+        rt.half = p->dh / 2;
+        rt.log2_theta = p->rope_theta > 0.f ? log2f(p->rope_theta) : 0.f;
+        const bool rope = p->rope_theta > 0.f;
+        cudaError_t e = tpk::rms_rows(x, p->dtype == TP_FP32, M, p->d, p->eps, r1, rope ? &rt : nullptr, st);
         if (e != cudaSuccess) return cuda_status(e);
         ex1.row_scale = r1;
-        ex1.rope = p->rope_theta > 0.f;
+        ex1.rope_cs = rope ? rt.cs : nullptr;
         ex1.rope_seq = seq;
-        ex1.rope_pos0 = cache_pos;
         ex2.row_scale = r2;
     }
     tp_status s = column_linear_impl(p, TP_QKV, x, M, packed, qkv, gs, gsb, ex1, st);
@@ -139,7 +148,7 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
     if (s != TP_OK) return s;
     if (p->llama) {  // RMSNorm of H: scale from the fp32 H, the GEMM reads its plan-dtype copy
-        cudaError_t e = tpk::rms_rows(hf32, 1, M, p->d, p->eps, r2, st);
+        cudaError_t e = tpk::rms_rows(hf32, 1, M, p->d, p->eps, r2, nullptr, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
     s = column_linear_impl(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, ex2, st);
@@ -337,12 +346,11 @@ static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M
         g.ldo = n_out;
         g.granule = p->granule;
         g.row_scale = ex.row_scale;
-        if (ex.rope) {
+        if (ex.rope_cs) {
             g.rope_cols = 2 * p->hl * p->dh;  // the Q and K heads of each shard's [Q | K | V] row
             g.rope_dh = p->dh;
             g.rope_seq = ex.rope_seq;
-            g.rope_pos0 = ex.rope_pos0;
-            g.rope_log2_theta = log2f(p->rope_theta);
+            g.rope_cs = ex.rope_cs;
         }
         if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, device_error_word(), st));
         if (tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32))
