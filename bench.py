@@ -575,6 +575,7 @@ def main():
                     help="instead of the headline line: only the decode leg (for profiling its kernels)")
     ap.add_argument("--decode-batch", type=int, default=1)
     ap.add_argument("--timeline", action="store_true", help="with --decode-only: per-kernel device timeline")
+    ap.add_argument("--prenorm", action="store_true", help="with --decode-only: the RMSNorm + RoPE block variant")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline line: one line per batch/prompt and tp-sweep workload")
     args = ap.parse_args()
@@ -587,7 +588,7 @@ def main():
     if args.decode_only:
         import torch
         print(json.dumps(bench_decode(args, torch.device("cuda", 0), batch=args.decode_batch,
-                                      timeline=args.timeline)), flush=True)
+                                      timeline=args.timeline, prenorm=args.prenorm)), flush=True)
         return 0
     return run_ours(args)
 

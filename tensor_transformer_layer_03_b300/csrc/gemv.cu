@@ -93,9 +93,51 @@ __device__ __forceinline__ void row_dots(const bf16* __restrict__ w, const bf16*
     }
 }
 
-// The same for two weight rows at once (w0 with inputs x0, w1 with x1):
-// their loads are issued together, 2 * GV_UNROLL in flight per lane.
-template <int MT>
+// 8 bf16 (one 16-byte chunk) to fp32: element 2i is the low half of word i.
+__device__ __forceinline__ void cvt8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Both rows' partial dot products with one 16-byte chunk of each: every
+// weight chunk is converted once for all MT input rows, and with SAME_X
+// (x0 == x1) every input chunk once for both weight rows.
+template <int MT, bool SAME_X>
+__device__ __forceinline__ void chunk_dots2(const uint4& a, const uint4& b, const bf16* __restrict__ x0,
+                                            const bf16* __restrict__ x1, long long ldx, int off, float (&acc0)[MT],
+                                            float (&acc1)[MT]) {
+    float fa[8], fb[8];
+    cvt8(a, fa);
+    cvt8(b, fb);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float xa[8], xb[8];
+        cvt8(__ldg(reinterpret_cast<const uint4*>(x0 + m * ldx + off)), xa);
+        if (SAME_X) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xb[j] = xa[j];
+        } else {
+            cvt8(__ldg(reinterpret_cast<const uint4*>(x1 + m * ldx + off)), xb);
+        }
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            s0 = fmaf(fa[j], xa[j], s0);
+            s1 = fmaf(fb[j], xb[j], s1);
+        }
+        acc0[m] += s0;
+        acc1[m] += s1;
+    }
+}
+
+// The same for two weight rows at once (w0 with inputs x0, w1 with x1;
+// SAME_X when x0 == x1): their loads are issued together, 2 * GV_UNROLL in
+// flight per lane.
+template <int MT, bool SAME_X>
 __device__ __forceinline__ void row_dots2(const bf16* __restrict__ w0, const bf16* __restrict__ x0,
                                           const bf16* __restrict__ w1, const bf16* __restrict__ x1, long long ldx,
                                           int K, float (&acc0)[MT], float (&acc1)[MT]) {
@@ -110,22 +152,11 @@ __device__ __forceinline__ void row_dots2(const bf16* __restrict__ w0, const bf1
             v1[u] = ld_stream(w1 + (c + 32 * u) * 8);
         }
 #pragma unroll
-        for (int u = 0; u < GV_UNROLL; ++u) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                acc0[m] += dot8(v0[u], __ldg(reinterpret_cast<const uint4*>(x0 + m * ldx + (c + 32 * u) * 8)));
-                acc1[m] += dot8(v1[u], __ldg(reinterpret_cast<const uint4*>(x1 + m * ldx + (c + 32 * u) * 8)));
-            }
-        }
+        for (int u = 0; u < GV_UNROLL; ++u)
+            chunk_dots2<MT, SAME_X>(v0[u], v1[u], x0, x1, ldx, (c + 32 * u) * 8, acc0, acc1);
     }
-    for (; c < nch; c += 32) {
-        const uint4 a = ld_stream(w0 + c * 8), b = ld_stream(w1 + c * 8);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            acc0[m] += dot8(a, __ldg(reinterpret_cast<const uint4*>(x0 + m * ldx + c * 8)));
-            acc1[m] += dot8(b, __ldg(reinterpret_cast<const uint4*>(x1 + m * ldx + c * 8)));
-        }
-    }
+    for (; c < nch; c += 32)
+        chunk_dots2<MT, SAME_X>(ld_stream(w0 + c * 8), ld_stream(w1 + c * 8), x0, x1, ldx, c * 8, acc0, acc1);
 }
 
 template <int MT, int EPI>
@@ -146,7 +177,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
             float ag[MT], au[MT];
 #pragma unroll
             for (int m = 0; m < MT; ++m) ag[m] = au[m] = 0.f;
-            row_dots2<MT>(W + gate_row * g.K, X, W + (gate_row + g.granule) * g.K, X, g.lda, g.K, ag, au);
+            row_dots2<MT, true>(W + gate_row * g.K, X, W + (gate_row + g.granule) * g.K, X, g.lda, g.K, ag, au);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const float rs = g.row_scale ? g.row_scale[m] : 1.f;  // pre-norm: 1/rms of input row m
@@ -164,7 +195,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
             float acc[2][MT];
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
-            row_dots2<MT>(W + (long long)it * g.K, X, W + (long long)(it + 1) * g.K, X, g.lda, g.K, acc[0], acc[1]);
+            row_dots2<MT, true>(W + (long long)it * g.K, X, W + (long long)(it + 1) * g.K, X, g.lda, g.K, acc[0], acc[1]);
             const int s = it / g.N, n = it % g.N;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
@@ -194,7 +225,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
             if (it2 < items)
-                row_dots2<MT>(W + (long long)it * g.K, X, W + (long long)it2 * g.K, X, g.lda, g.K, acc[0], acc[1]);
+                row_dots2<MT, true>(W + (long long)it * g.K, X, W + (long long)it2 * g.K, X, g.lda, g.K, acc[0], acc[1]);
             else
                 row_dots<MT>(W + (long long)it * g.K, X, g.lda, g.K, acc[0]);
 #pragma unroll
@@ -216,40 +247,55 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_col_k(GemvArgs g) {
 
 // row-parallel: out[m][n] = residual + sum_s <A_s[m][:], W_s[n][:]>
 template <int MT>
+__device__ __forceinline__ void row_store(const GemvArgs& g, int n, float (&acc)[MT]) {
+    const int lane = threadIdx.x % 32;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float v = warp_sum(acc[m]);
+        if (lane == 0) {
+            const long long o = (long long)m * g.ldo + n;
+            if (g.residual)
+                v += g.residual_f32 ? ((const float*)g.residual)[o] : __bfloat162float(((const bf16*)g.residual)[o]);
+            ((float*)g.out)[o] = v;
+            if (g.out2) ((bf16*)g.out2)[o] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
+// Row-parallel: a warp owns output features n and n + nw and walks row n
+// and row n + nw of every shard's weight block in shard order (the fused
+// all-reduce), both rows reading the same shard input.
+template <int MT>
 __global__ void __launch_bounds__(GV_THREADS) gemv_row_k(GemvArgs g) {
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = threadIdx.x / 32;
     const int gw = blockIdx.x * GV_WARPS + warp, nw = gridDim.x * GV_WARPS;
     const bf16* W = (const bf16*)g.W;
     const bf16* A = (const bf16*)g.A;
     pdl_launch_next();
     pdl_wait_prev();
-    for (int n = gw; n < g.N; n += nw) {
-        float acc[MT];
+    for (int n = gw; n < g.N; n += 2 * nw) {
+        const int n2 = n + nw;
+        float acc[MT], acc2[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-        // shards in order (the fused all-reduce), two rows' loads in flight
-        int s = 0;
-        for (; s + 1 < g.shards; s += 2) {
-            float a1[MT];
+        for (int m = 0; m < MT; ++m) acc[m] = acc2[m] = 0.f;
+        for (int s = 0; s < g.shards; ++s) {
+            const bf16* Ws = W + s * g.w_shard;
+            const bf16* As = A + s * g.a_shard;
+            float p[MT], p2[MT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) a1[m] = 0.f;
-            row_dots2<MT>(W + s * g.w_shard + (long long)n * g.K, A + s * g.a_shard,
-                          W + (s + 1) * g.w_shard + (long long)n * g.K, A + (s + 1) * g.a_shard, g.lda, g.K, acc, a1);
+            for (int m = 0; m < MT; ++m) p[m] = p2[m] = 0.f;
+            if (n2 < g.N)
+                row_dots2<MT, true>(Ws + (long long)n * g.K, As, Ws + (long long)n2 * g.K, As, g.lda, g.K, p, p2);
+            else
+                row_dots<MT>(Ws + (long long)n * g.K, As, g.lda, g.K, p);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m] += a1[m];
-        }
-        if (s < g.shards) row_dots<MT>(W + s * g.w_shard + (long long)n * g.K, A + s * g.a_shard, g.lda, g.K, acc);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float v = warp_sum(acc[m]);
-            if (lane == 0) {
-                const long long o = (long long)m * g.ldo + n;
-                if (g.residual)
-                    v += g.residual_f32 ? ((const float*)g.residual)[o] : __bfloat162float(((const bf16*)g.residual)[o]);
-                ((float*)g.out)[o] = v;
-                if (g.out2) ((bf16*)g.out2)[o] = __float2bfloat16_rn(v);
+            for (int m = 0; m < MT; ++m) {
+                acc[m] += p[m];
+                acc2[m] += p2[m];
             }
         }
+        row_store<MT>(g, n, acc);
+        if (n2 < g.N) row_store<MT>(g, n2, acc2);
     }
 }
 

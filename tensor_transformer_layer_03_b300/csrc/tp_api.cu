@@ -47,7 +47,7 @@ struct Workspace {
 // Stream-K scratch of the tensor-core GEMMs (bf16 plans, M past the
 // weight-streaming range); 0 when no GEMM of this shape would use it.
 size_t linear_scratch_bytes(const tp_plan_s* p, long long M) {
-    if (p->dtype != TP_BF16 || M <= tpk::GEMV_MAX_M) return 0;
+    if (p->dtype != TP_BF16 || M <= tpk::GEMV_PREFERRED_MAX_M) return 0;
     return tpk::tc_gemm_scratch_bytes();
 }
 
@@ -352,9 +352,10 @@ static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M
             g.rope_seq = ex.rope_seq;
             g.rope_cs = ex.rope_cs;
         }
-        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, device_error_word(), st));
-        if (tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32))
-            return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
+        const bool tc_ok = tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32);
+        if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok))
+            return cuda_status(tpk::gemv(g, device_error_word(), st));
+        if (tc_ok) return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
     if (ex.row_scale) return TP_ERR_UNSUPPORTED;  // (plan creation rules this out for pre-norm plans)
     tpk::SimtGemm g{};
@@ -411,9 +412,10 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
         g.out2 = out_act;
         g.residual = residual;
         g.residual_f32 = res_f32;
-        if (tpk::gemv_supported(g)) return cuda_status(tpk::gemv(g, device_error_word(), st));
-        if (tpk::tc_gemm_supported(M, p->d, ks))
-            return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
+        const bool tc_ok = tpk::tc_gemm_supported(M, p->d, ks);
+        if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok))
+            return cuda_status(tpk::gemv(g, device_error_word(), st));
+        if (tc_ok) return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
     }
     tpk::SimtGemm g{};
     g.epi = tpk::EPI_ROW_REDUCE;

@@ -48,7 +48,8 @@ def _decode_steps(shape, deg, B, P, n, seed):
 
 
 @pytest.mark.parametrize("B,shape,deg,P,n", [
-    (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 6),    # weight-streaming linears (M <= 8)
+    (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 6),    # weight-streaming linears (M <= 4)
+    (8, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 90, 3),     # tensor-core linears at 8 rows, split-K
     (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 5),   # tensor-core linears, split-K
     (64, I.BlockShape(512, 4, 1536, "swiglu"), 4, 70, 3),     # many sequences, one m-block
 ])

@@ -59,7 +59,7 @@ def test_llama7b_prefill(tp):
 
 
 @pytest.mark.parametrize("B,shape,deg,P,n", [
-    (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 5),    # weight-streaming linears (M <= 8)
+    (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 5),    # weight-streaming linears (M <= 4)
     (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 4),   # tensor-core linears
 ])
 def test_llama_multistep_decode(tp, B, shape, deg, P, n):
