@@ -100,6 +100,11 @@ constexpr int GEMV_MAX_M = 8;
 constexpr int GEMV_PREFERRED_MAX_M = 4;
 bool gemv_supported(const GemvArgs& g);
 cudaError_t gemv(const GemvArgs& g, int* dev_err, cudaStream_t st);
+// 2..8 rows with the products on the tensor cores (gemv_mma.cu): K a
+// multiple of 32, N a multiple of 16, SwiGLU granule a multiple of 16,
+// row-parallel launches with at most 8 shards.
+bool gemv_mma_supported(const GemvArgs& g);
+cudaError_t gemv_mma(const GemvArgs& g, cudaStream_t st);
 
 // ---- pre-norm helpers (norm.cu) ----------------------------------------------
 // W[r][c] *= gamma[c] for rows x d (plan dtype, rounded back to it).

@@ -352,6 +352,7 @@ static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M
             g.rope_seq = ex.rope_seq;
             g.rope_cs = ex.rope_cs;
         }
+        if (M >= 2 && M <= tpk::GEMV_MAX_M && tpk::gemv_mma_supported(g)) return cuda_status(tpk::gemv_mma(g, st));
         const bool tc_ok = tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32);
         if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok))
             return cuda_status(tpk::gemv(g, device_error_word(), st));
@@ -412,6 +413,7 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
         g.out2 = out_act;
         g.residual = residual;
         g.residual_f32 = res_f32;
+        if (M >= 2 && M <= tpk::GEMV_MAX_M && tpk::gemv_mma_supported(g)) return cuda_status(tpk::gemv_mma(g, st));
         const bool tc_ok = tpk::tc_gemm_supported(M, p->d, ks);
         if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok))
             return cuda_status(tpk::gemv(g, device_error_word(), st));

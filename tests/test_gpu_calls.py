@@ -25,6 +25,7 @@ SHAPES = [
     (4096, 32, 11008, 2, 1),
     (4096, 32, 11008, 8, 8),
     (512, 8, 1536, 4, 5),
+    (256, 4, 1056, 2, 3),    # 16-row gate/up blocks (d_ffn/tp = 528)
     # one-SM tiles (M <= 128) and the edge of the 256-row SM-pair tiles
     (512, 8, 1536, 2, 128),
     (1024, 8, 2816, 4, 100),
