@@ -1,4 +1,6 @@
-// Weight-streaming kernels for the small-M (decode) regime, bf16.
+// Weight-streaming kernels for the small-M (decode) regime, bf16, with the
+// products on the CUDA cores: the one-token-row step, and 2..8 rows where
+// the tensor-core streaming kernels (gemv_mma.cu) do not apply.
 //
 // With one to a few tokens per step every weight element is used M times, so
 // the linears are bound by reading the packed weights once from HBM.  Each

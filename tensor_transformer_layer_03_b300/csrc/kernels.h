@@ -93,10 +93,10 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch
 // ---- small-M weight streaming (gemv.cu): same arguments as the GEMM ---------
 typedef TcGemm GemvArgs;
 constexpr int GEMV_MAX_M = 8;
-// Above this many rows the tensor-core GEMM (split-K) is faster where it
-// applies: at 8 rows the streaming loop is bound by its conversions and
-// FMAs (7B decode step, one B300: 285 us at 8 rows vs 163 us at 16 rows on
-// the tensor cores; 142 us at 4 rows streaming).
+// Dispatch for 2..8 rows: gemv_mma where it applies; else this CUDA-core
+// loop up to this many rows and the tensor-core GEMM (split-K) above it --
+// at 8 rows the loop is bound by its conversions and FMAs (7B decode step,
+// one B300: 285 us at 8 rows vs 150 us on the tensor-core GEMM).
 constexpr int GEMV_PREFERRED_MAX_M = 4;
 bool gemv_supported(const GemvArgs& g);
 cudaError_t gemv(const GemvArgs& g, int* dev_err, cudaStream_t st);
