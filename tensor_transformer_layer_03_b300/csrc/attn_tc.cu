@@ -31,6 +31,7 @@
 // Every mbarrier wait is bounded (2 s of %globaltimer): on expiry the kernel
 // records a device error, raises a CTA abort flag, drains its MMAs and frees
 // TMEM before returning.
+#include <atomic>
 #include <math.h>
 
 #include "common.cuh"
@@ -423,13 +424,13 @@ bool make_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4], cons
 template <int D>
 cudaError_t attn_launch(const AttnArgs& a, int* dev_err, cudaStream_t st) {
     using C = Cfg<D>;
-    static bool attr[64] = {false};
+    static std::atomic<bool> attr[64];  // per device; racing first calls set the same attribute
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr[dev]) {
+    if (dev >= 0 && dev < 64 && !attr[dev].load()) {
         cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        attr[dev] = true;
+        attr[dev].store(true);
     }
     const uint64_t rowlen = 3ull * a.hl * D;
     const uint64_t M = (uint64_t)a.B * a.Tq;

@@ -31,6 +31,7 @@
 // raises a CTA-wide abort flag and leaves its loop; in-flight tensor-core
 // work is drained and TMEM freed before the CTA exits, and the two CTAs of a
 // pair leave together.
+#include <atomic>
 #include <cuda.h>
 
 #include "common.cuh"
@@ -612,12 +613,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 }
 
 int sm_count() {
-    static int n[64] = {0};
+    static std::atomic<int> n[64];  // per device; racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 148;
-    if (!n[dev]) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
-    return n[dev] > 0 ? n[dev] : 148;
+    int v = n[dev].load();
+    if (!v) {
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev].store(v);
+    }
+    return v > 0 ? v : 148;
 }
 
 }  // namespace
@@ -629,11 +634,11 @@ namespace {
 // Co-resident clusters of two for the paired kernel (an SM pair must come
 // from one GPC, so this can be below SMs / 2).
 int pair_slots() {
-    static int n[64] = {0};
+    static std::atomic<int> n[64];  // per device; racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 0;
-    if (!n[dev]) {
+    if (!n[dev].load()) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -650,21 +655,22 @@ int pair_slots() {
             cudaGetLastError();
             c = -1;
         }
-        n[dev] = c;
+        n[dev].store(c);
     }
-    return n[dev] > 0 ? n[dev] : 0;
+    const int v = n[dev].load();
+    return v > 0 ? v : 0;
 }
 
 template <bool PAIR>
 cudaError_t set_smem_attr() {
-    static bool done[64] = {false};
+    static std::atomic<bool> done[64];  // per device; racing first calls set the same attribute
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !done[dev]) {
+    if (dev >= 0 && dev < 64 && !done[dev].load()) {
         cudaError_t e =
             cudaFuncSetAttribute(tc_gemm_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<PAIR>::SMEM);
         if (e != cudaSuccess) return e;
-        done[dev] = true;
+        done[dev].store(true);
     }
     return cudaSuccess;
 }

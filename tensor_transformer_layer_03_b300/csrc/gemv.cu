@@ -23,6 +23,7 @@
 //  * row-parallel with the all-reduce fused in (same section): the warp that
 //    owns output feature n walks row n of every shard's weight block in
 //    shard order and sums the partial dot products in registers.
+#include <atomic>
 #include "common.cuh"
 #include "kernels.h"
 
@@ -302,12 +303,16 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_row_k(GemvArgs g) {
 }
 
 int sm_count_dev() {
-    static int n[64] = {0};
+    static std::atomic<int> n[64];  // per device; racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 148;
-    if (!n[dev]) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
-    return n[dev] > 0 ? n[dev] : 148;
+    int v = n[dev].load();
+    if (!v) {
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev].store(v);
+    }
+    return v > 0 ? v : 148;
 }
 
 // Grid: every warp gets the same number of items (ceil(items / warps)),

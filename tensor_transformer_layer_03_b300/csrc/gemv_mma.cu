@@ -22,6 +22,7 @@
 // all-reduce); its S warps split the k range (row-parallel: shard-major),
 // and warp 0 adds their partial tiles in warp order through shared memory
 // and runs the epilogue.  Launched with programmatic dependent launch.
+#include <atomic>
 #include "common.cuh"
 #include "kernels.h"
 
@@ -238,12 +239,16 @@ __global__ void __launch_bounds__(MMA_MAX_WARPS * 32) gemv_mma_row_k(GemvArgs g,
 }
 
 int sm_count_mma() {
-    static int n[64] = {0};
+    static std::atomic<int> n[64];  // per device; racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 148;
-    if (!n[dev]) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
-    return n[dev] > 0 ? n[dev] : 148;
+    int v = n[dev].load();
+    if (!v) {
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev].store(v);
+    }
+    return v > 0 ? v : 148;
 }
 
 cudaError_t launch(void (*kern)(GemvArgs, int), int blocks, int warps, cudaStream_t st, const GemvArgs& g, int arg) {

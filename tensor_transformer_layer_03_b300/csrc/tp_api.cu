@@ -3,6 +3,7 @@
 // Everything here runs on the host.  Calls validate their arguments before
 // enqueuing anything, then launch the kernels of pack.cu, simt.cu,
 // gemm_tc.cu, attn_tc.cu and decode.cu on the caller's stream.
+#include <atomic>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -30,14 +31,16 @@ tp_status cuda_status(cudaError_t e) { return tpk::status_from_cuda(e); }
 int* device_error_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    static int* addr[64] = {nullptr};
+    static std::atomic<int*> addr[64];  // per device; racing first calls store the same address
     if (dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
+    int* a = addr[dev].load();
+    if (!a) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_tp_device_error) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<int*>(p);
+        a = static_cast<int*>(p);
+        addr[dev].store(a);
     }
-    return addr[dev];
+    return a;
 }
 
 struct Workspace {
