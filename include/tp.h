@@ -31,7 +31,9 @@
  *    stream.  Every call only enqueues work and returns; results are ready
  *    when the stream reaches them.
  *  - Arguments are validated on the host before anything is enqueued; a call
- *    that returns an error has enqueued nothing.  Device pointers must be
+ *    that returns a validation error (any code but TP_ERR_CUDA) has enqueued
+ *    nothing -- the whole-block calls check every step's arguments before
+ *    their first launch.  Device pointers must be
  *    16-byte aligned (TP_ERR_ALIGNMENT otherwise).  Launch failures return
  *    TP_ERR_CUDA.  Device-side bounded waits that give up record a code that
  *    tp_sync_status() reports as TP_ERR_DEVICE_TIMEOUT.

@@ -84,6 +84,20 @@ size_t stack_workspace_bytes(const tp_plan_s* p, int batch, int seq) {
     return workspace_layout(p, batch, seq).total + 2 * align_up((size_t)batch * seq * p->d * p->esize, 1024);
 }
 
+// Argument checks of tp_attention_heads that need no buffer contents; the
+// whole-block calls run them before enqueuing anything.
+tp_status attention_check(const tp_plan_s* p, int batch, int seq_q, const void* k_cache, const void* v_cache,
+                          int cache_cap, int cache_pos) {
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq_q <= 0 || cache_pos < 0) return TP_ERR_INVALID_DIM;
+    const bool cached = k_cache != nullptr;
+    if (!cached && cache_pos != 0) return TP_ERR_INVALID_DIM;
+    if (cached && (cache_cap <= 0 || (long long)cache_pos + seq_q > cache_cap)) return TP_ERR_INVALID_DIM;
+    if (misaligned(k_cache) || misaligned(v_cache)) return TP_ERR_ALIGNMENT;
+    if (p->dh != 32 && p->dh != 64 && p->dh != 128) return TP_ERR_UNSUPPORTED;
+    return TP_OK;
+}
+
 }  // namespace
 
 // The block S1..S5 on a validated workspace layout; out_act (nullable)
@@ -448,15 +462,10 @@ tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int
                              void* v_cache, int cache_cap, int cache_pos, void* out_shards, void* scratch,
                              size_t scratch_bytes, void* stream) {
     if (!p || !qkv_shards || !out_shards) return TP_ERR_NULL_ARG;
-    if ((k_cache == nullptr) != (v_cache == nullptr)) return TP_ERR_NULL_ARG;
-    if (batch <= 0 || seq_q <= 0 || cache_pos < 0) return TP_ERR_INVALID_DIM;
+    if (misaligned(qkv_shards) || misaligned(out_shards) || misaligned(scratch)) return TP_ERR_ALIGNMENT;
+    const tp_status chk = attention_check(p, batch, seq_q, k_cache, v_cache, cache_cap, cache_pos);
+    if (chk != TP_OK) return chk;
     const bool cached = k_cache != nullptr;
-    if (!cached && cache_pos != 0) return TP_ERR_INVALID_DIM;
-    if (cached && (cache_cap <= 0 || (long long)cache_pos + seq_q > cache_cap)) return TP_ERR_INVALID_DIM;
-    if (misaligned(qkv_shards) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out_shards) ||
-        misaligned(scratch))
-        return TP_ERR_ALIGNMENT;
-    if (p->dh != 32 && p->dh != 64 && p->dh != 128) return TP_ERR_UNSUPPORTED;
     const size_t need = cached ? attn_scratch_bytes(p, batch, seq_q) : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     tpk::AttnArgs a{};
@@ -497,7 +506,9 @@ tp_status tp_block_forward(tp_plan_t p, const void* x, int batch, int seq, int c
                            size_t ws_bytes, void* out_f32, void* stream) {
     if (!p || !x || !packed || !workspace || !out_f32) return TP_ERR_NULL_ARG;
     if (batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
-    if (misaligned(workspace)) return TP_ERR_ALIGNMENT;
+    if (misaligned(workspace) || misaligned(x) || misaligned(packed) || misaligned(out_f32)) return TP_ERR_ALIGNMENT;
+    const tp_status chk = attention_check(p, batch, seq, k_cache, v_cache, cache_cap, cache_pos);
+    if (chk != TP_OK) return chk;
     const Workspace w = workspace_layout(p, batch, seq);
     if (ws_bytes < w.total) return TP_ERR_WORKSPACE_TOO_SMALL;
     return block_forward_impl(p, x, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, packed, workspace,
@@ -523,6 +534,11 @@ tp_status tp_stack_forward(tp_plan_t p, int n_layers, const void* const* packed_
         if (k_caches && (!k_caches[l] || !v_caches[l])) return TP_ERR_NULL_ARG;
     }
     if (misaligned(workspace) || misaligned(x) || misaligned(out_f32)) return TP_ERR_ALIGNMENT;
+    for (int l = 0; l < n_layers; ++l) {
+        const tp_status chk = attention_check(p, batch, seq, k_caches ? k_caches[l] : nullptr,
+                                              v_caches ? v_caches[l] : nullptr, cache_cap, cache_pos);
+        if (chk != TP_OK) return chk;
+    }
     if (ws_bytes < stack_workspace_bytes(p, batch, seq)) return TP_ERR_WORKSPACE_TOO_SMALL;
     const Workspace w = workspace_layout(p, batch, seq);
     // two plan-dtype activation buffers after the block workspace: layer l

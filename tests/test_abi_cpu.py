@@ -215,3 +215,31 @@ def test_llama_plan_rules_and_validation(tp):
     assert pw.value == pw0.value and ws.value >= ws0.value + 2 * 128 * 4
     tp.tp_plan_destroy(h)
     tp.tp_plan_destroy(h0)
+
+
+def test_whole_block_calls_validate_before_the_first_launch(tp):
+    """Errors of later steps (attention head width, cache bounds, operand
+    alignment) come back before anything is launched: on this GPU-less host
+    a launch attempt would report TP_ERR_CUDA instead."""
+    P = ctypes.c_void_p
+    good, odd = P(0x10000), P(0x10008)
+    B = tp.tp_block_forward
+    S = tp.tp_stack_forward
+    arr = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    code, h = _create(tp, 192, 4, 64, 2)  # d_head = 48: no attention kernel
+    assert code == 0
+    assert B(h, good, 1, 4, 1, None, None, 0, 0, good, good, 1 << 30, good, None) == 9
+    assert S(h, 2, arr, good, 1, 4, 1, None, None, 0, 0, good, 1 << 30, good, None) == 9
+    tp.tp_plan_destroy(h)
+    for create in (lambda: _create(tp, 256, 4, 1024, 2), lambda: _create_llama(tp, 256, 4, 1024, 2)):
+        code, h = create()
+        assert code == 0
+        assert B(h, good, 1, 4, 1, good, good, 5, 2, good, good, 1 << 30, good, None) == 2   # 2 + 4 > cap 5
+        assert B(h, good, 1, 4, 1, good, None, 8, 0, good, good, 1 << 30, good, None) == 1   # one-sided cache
+        assert B(h, good, 1, 4, 1, None, None, 0, 3, good, good, 1 << 30, good, None) == 2   # pos without cache
+        assert B(h, odd, 1, 4, 1, None, None, 0, 0, good, good, 1 << 30, good, None) == 7    # x
+        assert B(h, good, 1, 4, 1, odd, good, 8, 0, good, good, 1 << 30, good, None) == 7    # k cache
+        assert B(h, good, 1, 4, 1, None, None, 0, 0, odd, good, 1 << 30, good, None) == 7    # packed
+        assert B(h, good, 1, 4, 1, None, None, 0, 0, good, good, 1 << 30, odd, None) == 7    # out
+        assert S(h, 2, arr, good, 1, 4, 1, arr, arr, 5, 2, good, 1 << 30, good, None) == 2   # cache bounds
+        tp.tp_plan_destroy(h)
