@@ -63,7 +63,7 @@ typedef enum {
     TP_ERR_ALIGNMENT = 7,             /* pointer not 16-byte aligned, or a width
                                          not a multiple of 8 elements          */
     TP_ERR_WORKSPACE_TOO_SMALL = 8,
-    TP_ERR_UNSUPPORTED = 9,           /* valid plan, shape this build has no kernel for */
+    TP_ERR_UNSUPPORTED = 9,           /* valid plan, shape the library has no kernel for */
     TP_ERR_CUDA = 10,                 /* a CUDA runtime/launch error           */
     TP_ERR_DEVICE_TIMEOUT = 11        /* a device-side bounded wait gave up    */
 } tp_status;
@@ -91,7 +91,7 @@ const char* tp_last_cuda_error(void);
  *   tp_degree <= n_heads                   else TP_ERR_DEGREE_RANGE
  *   n_heads % tp_degree == 0               else TP_ERR_HEADS_NOT_DIVISIBLE
  *   d_ffn % tp_degree == 0                 else TP_ERR_FFN_NOT_DIVISIBLE
- * then the storage constraint of this build: d_model, d_head and d_ffn/tp
+ * then the library's storage constraint: d_model, d_head and d_ffn/tp
  * multiples of 8 (TP_ERR_ALIGNMENT), so that every row starts 16-byte
  * aligned.  An unknown act/dtype gives TP_ERR_UNSUPPORTED.
  * tp_plan_create uses SwiGLU and bf16.  On error *out is set to NULL.

@@ -66,7 +66,7 @@ def test_plan_rules_exhaustive_small(tp):
                     exp = o.check_plan(d, H, f, deg)
                     got = tp.status_name(code)
                     if exp == "OK":
-                        # this build additionally needs 8-element rows
+                        # the library additionally needs 8-element rows
                         dh, fl = d // H, f // deg
                         exp = "OK" if (d % 8 == 0 and dh % 8 == 0 and fl % 8 == 0) else "ALIGNMENT"
                     assert got == exp, (d, H, f, deg, got, exp)
