@@ -40,6 +40,10 @@
  *  - A plan is immutable after creation and may be used from several host
  *    threads and streams at once, provided calls in flight at the same time
  *    do not share output or workspace buffers.
+ *  - Tracing: every call that enqueues work opens an NVTX range named after
+ *    the call for its host duration; the whole-block calls add one range per
+ *    step ("S1 column QKV" ... "S5 row FFN-down + reduce", "RMSNorm(...)")
+ *    and per stacked layer, so profilers attribute each launch to its step.
  */
 #ifndef TP_H_
 #define TP_H_

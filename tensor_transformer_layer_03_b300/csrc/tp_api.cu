@@ -6,9 +6,12 @@
 #include <atomic>
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <new>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "kernels.h"
 #include "plan.h"
@@ -42,6 +45,16 @@ int* device_error_word() {
     }
     return a;
 }
+
+// NVTX range for the lifetime of a scope: every ABI call and every block
+// step shows up by name in nsys / ncu (--nvtx) timelines.  Without an
+// attached tool the push and pop are no-ops.
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
 
 struct Workspace {
     size_t qkv, attn, hf32, hact, u, scratch, gemm, rs, rope, total;
@@ -140,6 +153,7 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     float* r2 = r1 + M;
     ColumnExtras ex1, ex2;
     if (p->llama) {
+        const Range r("RMSNorm(X) + rotary table");
         // RMSNorm of x (its gain is in the packed QKV rows) and, in the same
         // launch, the rotary table of positions cache_pos + t, applied in
         // the QKV epilogue
@@ -157,19 +171,34 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
         ex1.rope_seq = seq;
         ex2.row_scale = r2;
     }
-    tp_status s = column_linear_impl(p, TP_QKV, x, M, packed, qkv, gs, gsb, ex1, st);
+    tp_status s;
+    {
+        const Range r("S1 column QKV");
+        s = column_linear_impl(p, TP_QKV, x, M, packed, qkv, gs, gsb, ex1, st);
+    }
     if (s != TP_OK) return s;
-    s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
-                           ptr_at(workspace, w.scratch), w.gemm - w.scratch, stream);
+    {
+        const Range r("S2 attention");
+        s = tp_attention_heads(p, qkv, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, attn,
+                               ptr_at(workspace, w.scratch), w.gemm - w.scratch, stream);
+    }
     if (s != TP_OK) return s;
-    s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
+    {
+        const Range r("S3 row O + reduce");
+        s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
+    }
     if (s != TP_OK) return s;
     if (p->llama) {  // RMSNorm of H: scale from the fp32 H, the GEMM reads its plan-dtype copy
+        const Range r("RMSNorm(H)");
         cudaError_t e = tpk::rms_rows(hf32, 1, M, p->d, p->eps, r2, nullptr, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    s = column_linear_impl(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, ex2, st);
+    {
+        const Range r("S4 column FFN-up");
+        s = column_linear_impl(p, TP_FFN_UP, hact, M, packed, u, gs, gsb, ex2, st);
+    }
     if (s != TP_OK) return s;
+    const Range r("S5 row FFN-down + reduce");
     return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, out_act, gs, gsb, stream);
 }
 
@@ -289,6 +318,7 @@ tp_status tp_linear_scratch_bytes(tp_plan_t p, int M, size_t* bytes) {
 tp_status tp_shard_weights(tp_plan_t p, const void* Wq, const void* Wk, const void* Wv, const void* Wo,
                            const void* W1_or_Wgate, const void* Wup, const void* Wdown, void* packed,
                            void* stream) {
+    const Range trace_("tp_shard_weights");
     if (!p || !Wq || !Wk || !Wv || !Wo || !W1_or_Wgate || !Wdown || !packed) return TP_ERR_NULL_ARG;
     if ((p->act == TP_ACT_SWIGLU) != (Wup != nullptr)) return TP_ERR_NULL_ARG;
     const void* all[] = {Wq, Wk, Wv, Wo, W1_or_Wgate, Wup, Wdown, packed};
@@ -307,6 +337,7 @@ tp_status tp_shard_weights(tp_plan_t p, const void* Wq, const void* Wk, const vo
 tp_status tp_shard_weights_llama(tp_plan_t p, const void* Wq, const void* Wk, const void* Wv, const void* Wo,
                                  const void* Wgate, const void* Wup, const void* Wdown, const void* g_attn,
                                  const void* g_ffn, void* packed, void* stream) {
+    const Range trace_("tp_shard_weights_llama");
     if (!p || !g_attn || !g_ffn) return TP_ERR_NULL_ARG;
     if (!p->llama) return TP_ERR_UNSUPPORTED;
     if (misaligned(g_attn) || misaligned(g_ffn)) return TP_ERR_ALIGNMENT;
@@ -324,6 +355,7 @@ tp_status tp_shard_weights_llama(tp_plan_t p, const void* Wq, const void* Wk, co
 
 tp_status tp_column_linear(tp_plan_t p, int which, const void* x, int M, const void* packed, void* out_shards,
                            void* scratch, size_t scratch_bytes, void* stream) {
+    const Range trace_("tp_column_linear");
     if (!p || !x || !packed || !out_shards) return TP_ERR_NULL_ARG;
     if (M <= 0 || (which != TP_QKV && which != TP_FFN_UP)) return TP_ERR_INVALID_DIM;
     if (misaligned(x) || misaligned(packed) || misaligned(out_shards) || misaligned(scratch))
@@ -402,6 +434,7 @@ extern "C" {
 tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
                                const void* residual, void* out_f32, void* out_act, void* scratch,
                                size_t scratch_bytes, void* stream) {
+    const Range trace_("tp_row_linear_reduce");
     if (!p || !in_shards || !packed || !out_f32) return TP_ERR_NULL_ARG;
     if (M <= 0 || (which != TP_ATTN_OUT && which != TP_FFN_DOWN)) return TP_ERR_INVALID_DIM;
     if (misaligned(in_shards) || misaligned(packed) || misaligned(residual) || misaligned(out_f32) ||
@@ -461,6 +494,7 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
 tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int seq_q, int causal, void* k_cache,
                              void* v_cache, int cache_cap, int cache_pos, void* out_shards, void* scratch,
                              size_t scratch_bytes, void* stream) {
+    const Range trace_("tp_attention_heads");
     if (!p || !qkv_shards || !out_shards) return TP_ERR_NULL_ARG;
     if (misaligned(qkv_shards) || misaligned(out_shards) || misaligned(scratch)) return TP_ERR_ALIGNMENT;
     const tp_status chk = attention_check(p, batch, seq_q, k_cache, v_cache, cache_cap, cache_pos);
@@ -504,6 +538,7 @@ tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int
 tp_status tp_block_forward(tp_plan_t p, const void* x, int batch, int seq, int causal, void* k_cache,
                            void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
                            size_t ws_bytes, void* out_f32, void* stream) {
+    const Range trace_("tp_block_forward");
     if (!p || !x || !packed || !workspace || !out_f32) return TP_ERR_NULL_ARG;
     if (batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
     if (misaligned(workspace) || misaligned(x) || misaligned(packed) || misaligned(out_f32)) return TP_ERR_ALIGNMENT;
@@ -525,6 +560,7 @@ tp_status tp_stack_workspace_bytes(tp_plan_t p, int batch, int seq, size_t* byte
 tp_status tp_stack_forward(tp_plan_t p, int n_layers, const void* const* packed_layers, const void* x, int batch,
                            int seq, int causal, void* const* k_caches, void* const* v_caches, int cache_cap,
                            int cache_pos, void* workspace, size_t ws_bytes, void* out_f32, void* stream) {
+    const Range trace_("tp_stack_forward");
     if (!p || !packed_layers || !x || !workspace || !out_f32) return TP_ERR_NULL_ARG;
     if (n_layers <= 0 || batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
     if ((k_caches == nullptr) != (v_caches == nullptr)) return TP_ERR_NULL_ARG;
@@ -546,6 +582,9 @@ tp_status tp_stack_forward(tp_plan_t p, int n_layers, const void* const* packed_
     const size_t act_bytes = align_up((size_t)batch * seq * p->d * p->esize, 1024);
     void* act[2] = {ptr_at(workspace, w.total), ptr_at(workspace, w.total + act_bytes)};
     for (int l = 0; l < n_layers; ++l) {
+        char name[32];
+        snprintf(name, sizeof name, "layer %d", l);
+        const Range r(name);
         const void* in = l == 0 ? x : act[(l - 1) % 2];
         void* copy = l + 1 < n_layers ? act[l % 2] : nullptr;
         const tp_status s =
