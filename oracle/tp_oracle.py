@@ -71,7 +71,7 @@ __all__ = [
     "linear", "gelu_erf", "silu", "softmax_rows", "attention_head",
     "multi_head_attention", "column_parallel_linear", "row_parallel_partials",
     "all_reduce_sum", "ffn", "block_forward", "sharded_block_forward",
-    "qkv_heads_of_shard", "stack_forward", "rms_norm", "rope", "llama_block_forward",
+    "stack_forward", "rms_norm", "rope", "fold_gains", "llama_block_forward",
 ]
 
 # ----------------------------------------------------------------------------
@@ -287,12 +287,6 @@ def block_forward(x, w: dict, n_heads: int, act: str, causal: bool,
     return Y, Kn, Vn
 
 
-def qkv_heads_of_shard(n_heads: int, tp: int, s: int) -> range:
-    """Heads owned by shard s ([TPT]: each shard owns a subset of heads)."""
-    h_l = n_heads // tp
-    return range(s * h_l, (s + 1) * h_l)
-
-
 def sharded_block_forward(x, w: dict, n_heads: int, act: str, causal: bool, tp: int):
     """The same block, computed shard by shard as [TPT] "the Original" lays it
     out: column-parallel Q/K/V by head, local attention over the shard's own
@@ -390,28 +384,39 @@ def rope(x, positions, n_heads: int, theta: float) -> np.ndarray:
     return x
 
 
+def fold_gains(w: dict, storage) -> dict:
+    """The weights with each norm gain folded into the columns that read the
+    normed rows: Wq, Wk, Wv times diag(g_attn) and Wg, Wu times diag(g_ffn),
+    each product stored once in ``storage``; the gains become 1.  In exact
+    arithmetic RMSNorm(x; g) W^T = (x / rms(x)) (W diag(g))^T, so only the
+    storage rounding of the products differs from the unfolded form."""
+    w = dict(w)
+    ga, gf = to64(w["g_attn"]), to64(w["g_ffn"])
+    for k in ("Wq", "Wk", "Wv"):
+        w[k] = _store(to64(w[k]) * ga[None, :], storage)
+    for k in ("Wg", "Wu"):
+        w[k] = _store(to64(w[k]) * gf[None, :], storage)
+    w["g_attn"], w["g_ffn"] = np.ones_like(ga), np.ones_like(gf)
+    return w
+
+
 def llama_block_forward(x, w: dict, n_heads: int, causal: bool, eps: float, theta: float,
-                        kcache=None, vcache=None, cache_pos: int = 0, storage=None):
+                        kcache=None, vcache=None, cache_pos: int = 0, storage=None, fold: bool = True):
     """Pre-norm block with RMSNorm (w["g_attn"], w["g_ffn"]) and RoPE (theta
     <= 0: none), SwiGLU FFN, tensor-parallel linears as in block_forward.
 
     x [B, T, d]; the T tokens sit at positions cache_pos..cache_pos+T-1.  The
     norm's 1/rms is taken from the unrounded input; ``storage="bf16"`` rounds
     the same points as block_forward (the normed operand of the FFN is the
-    rounded H times that scale) and stores each gain folded into the weight
-    columns that read the normed rows: W diag(g), rounded once, with the gain
-    then 1 (equal to the unfolded form in exact arithmetic).  Returns
+    rounded H times that scale) and, with ``fold`` (the default), stores each
+    gain folded into the weight columns that read the normed rows
+    (``fold_gains``: W diag(g), rounded once, gain then 1).  ``fold=False``
+    keeps the gains apart from the weights in storage mode too.  Returns
     (Y, K_new (rotated), V_new).
     """
     x = to64(x)
-    if storage is not None:
-        w = dict(w)
-        ga, gf = to64(w["g_attn"]), to64(w["g_ffn"])
-        for k in ("Wq", "Wk", "Wv"):
-            w[k] = _store(to64(w[k]) * ga[None, :], storage)
-        for k in ("Wg", "Wu"):
-            w[k] = _store(to64(w[k]) * gf[None, :], storage)
-        w["g_attn"], w["g_ffn"] = np.ones_like(ga), np.ones_like(gf)
+    if storage is not None and fold:
+        w = fold_gains(w, storage)
     B, T, d = x.shape
     dh = d // n_heads
     Y = np.empty((B, T, d))

@@ -100,11 +100,25 @@ def bf_block_seq(x, w, H, act, causal, kc=None, vc=None, P=0, rnd=None):
     return [[hres[t][c] + dn[t][c] for c in range(d)] for t in range(T)]
 
 
-def bf_llama_block_seq(x, w, H, causal, eps, theta, kc=None, vc=None, P=0):
+def bf_llama_block_seq(x, w, H, causal, eps, theta, kc=None, vc=None, P=0, rnd=None, r32=None, fold=False):
     """Pre-norm RMSNorm + RoPE block on one sequence with explicit loops:
-    every pair (2i, 2i+1) of a head rotated with math.cos / math.sin."""
+    every pair (2i, 2i+1) of a head rotated with math.cos / math.sin.
+
+    ``rnd`` (optional) rounds a scalar at the bf16 storage points (rotated
+    Q/K, V, attention output, the H operand, U) and ``r32`` the residual H;
+    with ``fold`` each gain is multiplied into the weight columns that read
+    the normed rows and every product is rounded by ``rnd`` on its own
+    (g[c] * W[o][c] element by element), the gains then being 1."""
     T, d = len(x), len(x[0])
     dh = d // H
+    r = rnd or (lambda v: v)
+    f32 = r32 or (lambda v: v)
+    if fold:
+        w = dict(w)
+        for n, gk in (("Wq", "g_attn"), ("Wk", "g_attn"), ("Wv", "g_attn"), ("Wg", "g_ffn"), ("Wu", "g_ffn")):
+            w[n] = [[r(row[c] * w[gk][c]) for c in range(len(row))] for row in w[n]]
+        w["g_attn"] = [1.0] * d
+        w["g_ffn"] = [1.0] * d
 
     def norm(rows, g):
         out = []
@@ -130,9 +144,9 @@ def bf_llama_block_seq(x, w, H, causal, eps, theta, kc=None, vc=None, P=0):
         return out
 
     xn = norm(x, w["g_attn"])
-    q = rot(bf_matvec_rows(xn, w["Wq"]))
-    k = rot(bf_matvec_rows(xn, w["Wk"]))
-    v_ = bf_matvec_rows(xn, w["Wv"])
+    q = [[r(v) for v in row] for row in rot(bf_matvec_rows(xn, w["Wq"]))]
+    k = [[r(v) for v in row] for row in rot(bf_matvec_rows(xn, w["Wk"]))]
+    v_ = [[r(v) for v in row] for row in bf_matvec_rows(xn, w["Wv"])]
     keys, vals = [], []
     for p in range(P):
         keys.append([kc[h][p][c] for h in range(H) for c in range(dh)])
@@ -149,12 +163,19 @@ def bf_llama_block_seq(x, w, H, causal, eps, theta, kc=None, vc=None, P=0):
             z = sum(e)
             for c in range(dh):
                 a[i][h * dh + c] = sum(e[n] * vals[js[n]][h * dh + c] for n in range(len(js))) / z
+    a = [[r(v) for v in row] for row in a]
     o_ = bf_matvec_rows(a, w["Wo"])
-    hres = [[x[t][c] + o_[t][c] for c in range(d)] for t in range(T)]
-    hn = norm(hres, w["g_ffn"])
+    hexact = [[x[t][c] + o_[t][c] for c in range(d)] for t in range(T)]
+    hres = [[f32(v) for v in row] for row in hexact]
+    # the FFN's norm: 1/rms of the residual H, applied to H's bf16 copy
+    hn = []
+    for t in range(T):
+        ms = sum(v * v for v in hres[t]) / d
+        sc = 1.0 / math.sqrt(ms + eps)
+        hn.append([r(hexact[t][c]) * sc * w["g_ffn"][c] for c in range(d)])
     g = bf_matvec_rows(hn, w["Wg"])
     u_ = bf_matvec_rows(hn, w["Wu"])
-    u = [[bf_silu(g[t][n]) * u_[t][n] for n in range(len(g[0]))] for t in range(T)]
+    u = [[r(bf_silu(g[t][n]) * u_[t][n]) for n in range(len(g[0]))] for t in range(T)]
     dn = bf_matvec_rows(u, w["Wd"])
     return [[hres[t][c] + dn[t][c] for c in range(d)] for t in range(T)]
 
@@ -450,6 +471,57 @@ def pin_llama_brute_force(o):
             ref = np.array(bf_llama_block_seq(x[b].tolist(), wl, H, causal, 1e-5, theta,
                                               kc[b].tolist() if P else None, vc[b].tolist() if P else None, P))
             assert np.max(np.abs(Y[b] - ref)) < 1e-11, (causal, theta, P)
+
+
+def pin_llama_brute_force_bf16_storage(o):
+    """The pre-norm block's bf16 storage mode equals explicit loops with
+    torch's bf16 cast at the same points: each gain folded into its weight
+    columns and every product rounded once, rotated Q/K and V, the attention
+    output, H's operand copy and U rounded, H itself kept in fp32.  With
+    ``fold=False`` the gains stay apart from the weights."""
+    def rnd(v):
+        return float(torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).double())
+
+    def r32(v):
+        return float(torch.tensor(v, dtype=torch.float64).to(torch.float32).double())
+    for causal, theta, P, fold in ((True, 10000.0, 0, True), (True, 500.0, 3, True), (False, 0.0, 0, True),
+                                   (True, 10000.0, 2, False)):
+        rng = _rng(61 + P + int(theta) % 5 + 7 * fold)
+        B, T, d, H, f, cap = 1, 4, 8, 2, 6, 7
+        w = _llama_weights(rng, d, f)
+        x = rng.standard_normal((B, T, d))
+        kc = rng.standard_normal((B, H, cap, d // H))
+        vc = rng.standard_normal((B, H, cap, d // H))
+        kw = dict(kcache=kc, vcache=vc, cache_pos=P) if P else {}
+        Y, _, _ = o.llama_block_forward(x, w, H, causal, 1e-5, theta, storage="bf16", fold=fold, **kw)
+        wl = {n: a.tolist() for n, a in w.items()}
+        ref = np.array(bf_llama_block_seq(x[0].tolist(), wl, H, causal, 1e-5, theta,
+                                          kc[0].tolist() if P else None, vc[0].tolist() if P else None, P,
+                                          rnd=rnd, r32=r32, fold=fold))
+        # H is an fp32 residual: compare at fp32 resolution
+        assert np.max(np.abs(Y[0] - ref)) < 1e-5 * max(1.0, np.max(np.abs(ref))), (causal, theta, P, fold)
+        Y0, _, _ = o.llama_block_forward(x, w, H, causal, 1e-5, theta, **kw)
+        assert np.max(np.abs(Y - Y0)) > 1e-4  # the mode really rounds
+    # folding changes only the rounding: without storage the two forms agree
+    rng = _rng(69)
+    w = _llama_weights(rng, 8, 6)
+    x = rng.standard_normal((1, 3, 8))
+    Ya, _, _ = o.llama_block_forward(x, w, 2, True, 1e-5, 10000.0)
+    wf = o.fold_gains(w, None)
+    assert np.max(np.abs(wf["g_attn"] - 1.0)) == 0.0 and np.max(np.abs(wf["g_ffn"] - 1.0)) == 0.0
+    Yb, _, _ = o.llama_block_forward(x, wf, 2, True, 1e-5, 10000.0)
+    assert np.max(np.abs(Ya - Yb)) < 1e-12
+
+
+def pin_round_fp32(o):
+    """Round to fp32, nearest even: 1 + 2^-24 is a tie that goes down to 1,
+    1 + 3 * 2^-24 goes up to 1 + 2^-22; against torch's float64 -> float32 cast."""
+    got = o.round_fp32(np.array([1 + 2.0 ** -24, 1 + 3 * 2.0 ** -24, -(1 + 2.0 ** -24), 0.1, 0.0]))
+    assert got[0] == 1.0 and got[1] == 1 + 2.0 ** -22 and got[2] == -1.0 and got[4] == 0.0
+    assert got[3] != 0.1 and abs(got[3] - 0.1) < 2.0 ** -27
+    x = _rng(17).standard_normal(100000) * np.exp(_rng(18).uniform(-30, 30, 100000))
+    ref = torch.from_numpy(x).to(torch.float32).double().numpy()
+    assert np.array_equal(o.round_fp32(x), ref)
 
 
 def pin_rope_properties(o):

@@ -4,7 +4,8 @@ tiles and split-K), with and without rotation, the 7B shape, multi-step
 decode with a growing cache on the weight-streaming and tensor-core linears,
 and a two-layer stack.  Bounds as in test_gpu_block.py: normwise <= 2e-2
 against the exact oracle, mean abs against the oracle's bf16-storage floor
-(which stores the gains folded into the bf16 weights, as the library does)."""
+(which stores the gains folded into the bf16 weights, as the library does),
+and, printed beside it, against the floor with the gains kept apart."""
 import pytest
 import torch
 
@@ -25,9 +26,31 @@ def _weights(shape, seed):
     return w, g
 
 
-def _check(got, ex, st, what):
+# Folding the gains into the bf16 weights adds one rounding per weight: on
+# the CPU it raised the bf16-storage floor by 1.28-1.32x over the unfolded
+# form at these shapes, so the output is also held to the unfolded floor
+# times this allowance on top of FLOOR_FACTOR.
+FOLD_ALLOWANCE = 1.35
+
+
+def _check(got, ex, st, what, st_unfolded=None):
     floor = mean_abs(st, ex)
-    return assert_close_bf16(got, ex, what, mean_abs_bound=max(BF16_MEAN_ABS, FLOOR_FACTOR * floor))
+    nw, ma = assert_close_bf16(got, ex, what, mean_abs_bound=max(BF16_MEAN_ABS, FLOOR_FACTOR * floor))
+    if st_unfolded is not None:
+        floor_u = mean_abs(st_unfolded, ex)
+        print(f"{what}: mean abs {ma:.3e}; floor folded {floor:.3e} ({ma / floor:.2f}x), "
+              f"unfolded {floor_u:.3e} ({ma / floor_u:.2f}x); folding alone {floor / floor_u:.2f}x")
+        bound_u = max(BF16_MEAN_ABS, FLOOR_FACTOR * FOLD_ALLOWANCE * floor_u)
+        assert ma <= bound_u, f"{what}: mean abs {ma:.3e} above the unfolded floor bound {bound_u:.3e}"
+    return nw, ma
+
+
+def _oracles(x, w, H, causal, theta, **kw):
+    """Exact, bf16-storage (gains folded) and bf16-storage (gains apart)."""
+    ex, K, V = o.llama_block_forward(x, w, H, causal, EPS, theta, **kw)
+    st, _, _ = o.llama_block_forward(x, w, H, causal, EPS, theta, storage="bf16", **kw)
+    su, _, _ = o.llama_block_forward(x, w, H, causal, EPS, theta, storage="bf16", fold=False, **kw)
+    return ex, st, su, K
 
 
 @pytest.mark.parametrize("shape,deg,B,T,theta", [
@@ -41,9 +64,8 @@ def test_llama_prefill(tp, shape, deg, B, T, theta):
     blk = TPBlock(shape, deg, "bf16", w, device=DEV, max_batch=B, max_seq=T, rms_eps=EPS, rope_theta=theta)
     y = blk.forward(x.to(DEV), True).cpu()
     blk.plan.sync_status()
-    ex, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, theta)
-    st, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, theta, storage="bf16")
-    _check(y, ex, st, f"pre-norm prefill d={shape.d_model} theta={theta}")
+    ex, st, su, _ = _oracles(x, w, shape.n_heads, True, theta)
+    _check(y, ex, st, f"pre-norm prefill d={shape.d_model} theta={theta}", su)
 
 
 def test_llama7b_prefill(tp):
@@ -53,9 +75,8 @@ def test_llama7b_prefill(tp):
     blk = TPBlock(shape, 2, "bf16", w, device=DEV, max_batch=B, max_seq=T, rms_eps=EPS, rope_theta=10000.0)
     y = blk.forward(x.to(DEV), True).cpu()
     blk.plan.sync_status()
-    ex, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, 10000.0)
-    st, _, _ = o.llama_block_forward(x, w, shape.n_heads, True, EPS, 10000.0, storage="bf16")
-    _check(y, ex, st, "7B pre-norm prefill")
+    ex, st, su, _ = _oracles(x, w, shape.n_heads, True, 10000.0)
+    _check(y, ex, st, "7B pre-norm prefill", su)
 
 
 @pytest.mark.parametrize("B,shape,deg,P,n", [
@@ -80,9 +101,8 @@ def test_llama_multistep_decode(tp, B, shape, deg, P, n):
           for i in range(n)]
     blk.plan.sync_status()
     got = torch.cat(ys, dim=1)
-    ex, K, _ = o.llama_block_forward(x, w, H, True, EPS, theta, kcache=kc, vcache=vc, cache_pos=P)
-    st, _, _ = o.llama_block_forward(x, w, H, True, EPS, theta, kcache=kc, vcache=vc, cache_pos=P, storage="bf16")
-    _check(got, ex, st, f"pre-norm {n}-step decode B={B}")
+    ex, st, su, K = _oracles(x, w, H, True, theta, kcache=kc, vcache=vc, cache_pos=P)
+    _check(got, ex, st, f"pre-norm {n}-step decode B={B}", su)
     kn = kd.cpu()
     assert torch.isnan(kn[:, :, P + n:]).all(), "cache rows past the last step were written"
     # keys are stored rotated: bf16 of the oracle's rotated K, within the
@@ -102,8 +122,9 @@ def test_llama_stack_prefill(tp):
     y = stk.forward(x.to(DEV), True).cpu()
     stk.plan.sync_status()
     outs = []
-    for storage in (None, "bf16"):
-        h, _, _ = o.llama_block_forward(x, w0, shape.n_heads, True, EPS, theta, storage=storage)
-        h, _, _ = o.llama_block_forward(o.round_bf16(h), w1, shape.n_heads, True, EPS, theta, storage=storage)
+    for storage, fold in ((None, True), ("bf16", True), ("bf16", False)):
+        h, _, _ = o.llama_block_forward(x, w0, shape.n_heads, True, EPS, theta, storage=storage, fold=fold)
+        h, _, _ = o.llama_block_forward(o.round_bf16(h), w1, shape.n_heads, True, EPS, theta, storage=storage,
+                                        fold=fold)
         outs.append(h)
-    _check(y, outs[0], outs[1], "2-layer pre-norm stack")
+    _check(y, outs[0], outs[1], "2-layer pre-norm stack", outs[2])

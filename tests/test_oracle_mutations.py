@@ -11,7 +11,7 @@ from pins import ALL_PINS
 real = {n: getattr(o, n) for n in ("attention_head", "linear", "silu", "gelu_erf", "all_reduce_sum",
                                    "block_forward", "round_bf16", "check_plan", "multi_head_attention",
                                    "softmax_rows", "row_parallel_partials", "column_parallel_linear",
-                                   "sharded_block_forward", "stack_forward", "rope", "rms_norm")}
+                                   "sharded_block_forward", "stack_forward", "rope", "rms_norm", "fold_gains")}
 
 
 def _att_scale_dh(q, k, v, causal, q_pos0=0):
@@ -145,7 +145,29 @@ def _rms_mean_abs(x, g, eps):
     return x / (np.mean(np.abs(x), axis=-1, keepdims=True) + eps) * g
 
 
+def _fold_unrounded(w, storage):
+    # the gain folded into the weights, but the product never stored in bf16
+    return real["fold_gains"](w, None)
+
+
+def _fold_round_twice(w, storage):
+    # the weights rounded once more before the gain is folded in
+    w = dict(w)
+    for k in ("Wq", "Wk", "Wv", "Wg", "Wu"):
+        w[k] = o.round_bf16(w[k])
+    return real["fold_gains"](w, storage)
+
+
+def _fold_attn_gain_on_ffn(w, storage):
+    # the attention norm's gain folded into the FFN's gate/up columns too
+    w = dict(w, g_ffn=w["g_attn"])
+    return real["fold_gains"](w, storage)
+
+
 MUTATIONS = {
+    "folded gain not rounded": ("fold_gains", _fold_unrounded),
+    "weights rounded before folding": ("fold_gains", _fold_round_twice),
+    "attention gain folded into the FFN": ("fold_gains", _fold_attn_gain_on_ffn),
     "rope pairs (i, i + d/2)": ("rope", _rope_half),
     "rope angle sign": ("rope", _rope_neg),
     "rms norm without eps": ("rms_norm", _rms_no_eps),
