@@ -148,11 +148,21 @@ tp_status tp_shard_weights(tp_plan_t plan, const void* Wq, const void* Wk, const
  *      TP_FFN_UP: n_s = d_ffn/tp, the activated U_s = silu(x Wg_s^T) *
  *                 (x Wu_s^T) (SwiGLU) or gelu(x W1_s^T) (GELU, erf form).
  *   scratch    device, nullable, scratch_bytes >= tp_linear_scratch_bytes(M)
- *              to be used.  With it, a GEMM whose output tiles would leave
- *              SMs idle in the last wave splits the reduction evenly over
- *              all SMs (stream-K: fp32 partial sums of split tiles pass
- *              through the scratch).  Contents on entry are ignored; calls
- *              in flight at the same time need separate scratch.
+ *              to be used; ZERO-FILLED before its first use (e.g. by
+ *              cudaMemset), and every call that completes leaves its
+ *              counters at zero again, so it can be reused without
+ *              clearing (also across CUDA graph replays).  With it, a
+ *              tensor-core GEMM whose output tiles would leave SMs idle in
+ *              the last wave cuts each tile of that wave into equal
+ *              k-parts on different SMs (run before the whole tiles): every
+ *              part writes its fp32 partial sums to the scratch and counts
+ *              itself in; at the end of its SM's work (bounded wait for the
+ *              tile's other parts) each part adds the partials of its own
+ *              rows of the tile in part order 0, 1, ... and applies the
+ *              epilogue -- inside the same launch, with no second pass.
+ *              Calls in flight at the same time need separate
+ *              scratch.  After tp_sync_status() reported
+ *              TP_ERR_DEVICE_TIMEOUT, zero-fill the scratch again.
  * M >= 1.
  */
 tp_status tp_column_linear(tp_plan_t plan, int which, const void* x, int M,
@@ -173,9 +183,10 @@ tp_status tp_column_linear(tp_plan_t plan, int which, const void* x, int M,
  *   out_f32    device fp32 [M, d]
  *   out_act    device act [M, d], nullable: a copy of out_f32 in the plan
  *              dtype (the operand of the next column-parallel linear)
- *   scratch    as in tp_column_linear.  With stream-K, the k-blocks of one
- *              output tile (all shards' partials) are split between SMs and
- *              their fp32 sums added in a fixed order by the tile's owner.
+ *   scratch    as in tp_column_linear.  When a tile is cut into parts, a
+ *              part spans consecutive k-blocks of the shard-major reduction
+ *              (so it may cover several shards' partials), and the parts'
+ *              fp32 sums are added in part order.
  */
 tp_status tp_row_linear_reduce(tp_plan_t plan, int which, const void* in_shards, int M,
                                const void* packed, const void* residual, void* out_f32,
@@ -225,7 +236,8 @@ tp_status tp_attention_heads(tp_plan_t plan, const void* qkv_shards, int batch, 
  * fit in it, else TP_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued.
  *  - The first call on each device looks up that array's device address
  *    (cudaGetSymbolAddress, with the device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process and does not survive cudaDeviceReset().
  *  - All calls on a device share the one array, so calls that can overlap
  *    on the GPU (different streams, no ordering between them) race and give
  *    wrong results; order them on one stream or with events.
@@ -242,7 +254,10 @@ tp_status tp_attention_decode_noalloc(tp_plan_t plan, const void* qkv_shards, in
  *   x         device act [batch*seq][d_model]
  *   k_cache/v_cache/cache_cap/cache_pos   as in tp_attention_heads
  *   packed    device, from tp_shard_weights
- *   workspace device, ws_bytes >= tp_plan_sizes(batch, seq) workspace bytes
+ *   workspace device, ws_bytes >= tp_plan_sizes(batch, seq) workspace bytes,
+ *             zero-filled before its first use (it holds the linears'
+ *             scratch, see tp_column_linear); calls that complete leave it
+ *             reusable without clearing
  *   out_f32   device fp32 [batch*seq][d_model] = Y
  */
 tp_status tp_block_forward(tp_plan_t plan, const void* x, int batch, int seq, int causal,
@@ -262,7 +277,8 @@ tp_status tp_block_forward(tp_plan_t plan, const void* x, int batch, int seq, in
  *   packed_layers  host array of n_layers device pointers (tp_shard_weights)
  *   k_caches, v_caches  host arrays of n_layers device caches (as in
  *                  tp_attention_heads) or both NULL
- *   workspace      device, ws_bytes >= tp_stack_workspace_bytes(batch, seq)
+ *   workspace      device, ws_bytes >= tp_stack_workspace_bytes(batch, seq),
+ *                  zero-filled before its first use (as for tp_block_forward)
  */
 tp_status tp_stack_workspace_bytes(tp_plan_t plan, int batch, int seq, size_t* bytes);
 tp_status tp_stack_forward(tp_plan_t plan, int n_layers, const void* const* packed_layers, const void* x,
@@ -305,8 +321,44 @@ tp_status tp_shard_weights_llama(tp_plan_t plan, const void* Wq, const void* Wk,
  * Wait for `stream`, then report (and clear) the first device-side error
  * recorded by a bounded wait in this library's kernels on the current
  * device: TP_ERR_DEVICE_TIMEOUT, TP_ERR_CUDA on a CUDA error, else TP_OK.
+ * After TP_ERR_DEVICE_TIMEOUT the outputs of the calls since the last
+ * check are undefined and linear scratch / block workspaces they used must
+ * be zero-filled again.  The device address of the error word (like that of
+ * tp_attention_decode_noalloc's array) is looked up once per device and
+ * kept for the life of the process: it does not survive cudaDeviceReset().
  */
 tp_status tp_sync_status(void* stream);
+
+/*
+ * Limit of every bounded device-side wait (mbarrier waits of the
+ * tensor-core kernels, the split-tile counters of the linears), in
+ * nanoseconds of %globaltimer, for launches enqueued after the call; 0
+ * restores the default of 2 s.  A wait that runs out records the error
+ * tp_sync_status() reports, and its kernel leaves early with its tensor
+ * memory freed.  Meant for tests of that failure path (a short limit makes
+ * waits run out); process-wide, not tied to a plan.
+ */
+void tp_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * Host-only description (no GPU needed) of how tp_column_linear (which =
+ * TP_QKV / TP_FFN_UP, row = 0) or tp_row_linear_reduce (which =
+ * TP_ATTN_OUT / TP_FFN_DOWN, row = 1) would run M token rows with a linear
+ * scratch of scratch_bytes, on a GPU with `sms` SMs of which `pair_slots`
+ * SM pairs fit at once (148 and 74 on a B300).  kernel: 0 tensor-core
+ * GEMM, 1 weight streaming on the tensor cores (2..8 rows), 2 weight
+ * streaming on the CUDA cores, 3 fp32 CUDA-core GEMM.  For kernel 0: tiles
+ * (256 x 256 on SM pairs when paired, else 128 x 256), k-blocks of 64 per
+ * tile, the tiles run whole, the parts each remaining tile is cut into
+ * (the parts run first), the work items, the units launched and the bytes
+ * of scratch the launch touches (<= scratch_bytes).
+ */
+typedef struct {
+    int kernel, paired, tiles, k_blocks_per_tile, whole_tiles, parts, items, units;
+    size_t scratch_bytes_touched;
+} tp_linear_schedule_t;
+tp_status tp_linear_schedule(tp_plan_t plan, int row, int which, int M, size_t scratch_bytes, int sms,
+                             int pair_slots, tp_linear_schedule_t* out);
 
 #ifdef __cplusplus
 }

@@ -50,7 +50,6 @@ constexpr int AT_SLOTS = 5;    // K/V ring slots
 constexpr int AT_THREADS = 320;
 constexpr int HALF_BYTES = 128 * 64 * 2;  // one 128-row x 64-column swizzled half tile
 constexpr float RESCALE_LOG2 = 8.0f;      // rescale O only when the max grows by > 2^8
-constexpr unsigned long long AT_TIMEOUT_NS = 2000000000ull;
 
 template <int D>
 struct Cfg {
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const uint32_t a = smem_u32(drain);
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(a, 0)) {
-                if (globaltimer() - t0 > p.timeout_ns) {
+                if (globaltimer() - t0 > drain_limit_ns(p.timeout_ns)) {
                     record_error(p.err, DEV_ERR_TIMEOUT);
                     break;
                 }
@@ -465,7 +464,7 @@ cudaError_t attn_launch(const AttnArgs& a, int* dev_err, cudaStream_t st) {
     p.out_shard = (long long)M * a.hl * D;
     p.out_ld = a.hl * D;
     p.err = dev_err;
-    p.timeout_ns = AT_TIMEOUT_NS;
+    p.timeout_ns = wait_timeout_ns();
     const long long grid = (long long)p.n_pairs * a.H * a.B;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     attn_tc_kernel<D><<<(unsigned)grid, AT_THREADS, C::SMEM, st>>>(mq, mk, mv, p);

@@ -9,7 +9,7 @@
 //   blocks of the input and row blocks of the weight, partials summed):
 //       out[m][n] = residual[m][n] + sum_s sum_k A[s][m][k] * W[s][n][k]
 //       -- every shard's partial product is accumulated, in shard order, into
-//       the same TMEM accumulator, so no partial is ever written to memory.
+//       the same TMEM accumulator.
 //
 // Two variants of one persistent kernel (one CTA per SM, 192 threads):
 //  * PAIR (M > 128): clusters of two CTAs on neighbouring SMs compute a
@@ -24,13 +24,25 @@
 //            tcgen05.mma kind::f16, K = 16 steps, into one of two 256-column
 //            fp32 TMEM accumulators;
 //   warps 2-5 epilogue: tcgen05.ld of the finished accumulator (each warp its
-//            32-lane quarter), activation / residual, stores to global.
-// The epilogue of tile i overlaps the main loop of tile i+1 (two TMEM
-// accumulators = all 512 columns).  Every mbarrier wait is bounded: after
-// `timeout_ns` the waiting role records TP_ERR_DEVICE_TIMEOUT's device code,
-// raises a CTA-wide abort flag and leaves its loop; in-flight tensor-core
-// work is drained and TMEM freed before the CTA exits, and the two CTAs of a
-// pair leave together.
+//            32-lane quarter), through a per-warp shared staging block so
+//            that global stores are row-contiguous, activation / residual.
+// The epilogue of item i overlaps the main loop of item i+1 (two TMEM
+// accumulators = all 512 columns).
+//
+// Work decomposition: when the output tiles do not fill every unit (SM pair
+// or SM) in the last round, the tiles that fill whole rounds run whole and
+// each remaining tile is cut into `parts` equal k-ranges on different
+// units; the parts run first, the whole tiles after them.  A part writes its raw fp32 sums to the caller's scratch, counts
+// itself in (per tile, CTA and warp quarter), waits (bounded) for the
+// tile's other parts, and then reduces its own share of the tile's rows
+// over all parts, in part order, and runs the epilogue on them -- the
+// split reduction happens inside this launch, spread over the parts.  The
+// counters go back to zero when the last part leaves.
+//
+// Every wait is bounded: after `timeout_ns` the waiting role records
+// TP_ERR_DEVICE_TIMEOUT's device code, raises a CTA-wide abort flag and
+// leaves its loop; in-flight tensor-core work is drained and TMEM freed
+// before the CTA exits, and the two CTAs of a pair leave together.
 #include <atomic>
 #include <cuda.h>
 
@@ -49,9 +61,17 @@ namespace {
 constexpr int BN = 256, BK = 64;          // output columns per tile, K per stage
 constexpr int A_ROWS = 128;                // A rows staged per CTA
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 192;
-constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s
+constexpr int EPI_WARPS = 8;               // two per TMEM lane quarter, one per 128-column half
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int HALF_N = BN / 2;             // columns per epilogue warp
+constexpr int STG_FLOATS = 32 * 32;        // one epilogue warp's 32 x 32 staging block
+constexpr int STG_BYTES = EPI_WARPS * STG_FLOATS * 4;
+constexpr int PART_FLOATS = 32 * HALF_N;   // one warp's 32 rows x 128 columns of a split partial
+constexpr int SPLIT_ROUNDS_MAX = 4;        // split parts per unit at most
+constexpr int FIX_BYTES = 24 * 1024;       // each epilogue warp's share of the idle ring at the end of the work
 
+template <bool PAIR>
+struct GCfg;
 template <bool PAIR>
 struct GCfg {
     static constexpr int TILE_M = PAIR ? 256 : 128;   // output rows per tile
@@ -60,9 +80,11 @@ struct GCfg {
     static constexpr int STAGE_BYTES = A_BYTES + W_ROWS * BK * 2;
     static constexpr int STAGES = PAIR ? TP_GEMM_PAIR_STAGES : 4;
     static constexpr int GROUP_M = PAIR ? 8 : 16;       // row blocks per raster band (2048 rows)
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int RANKS = PAIR ? 2 : 1;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + STG_BYTES + 1024 + 256;
     // instruction descriptor: D fp32, A/B bf16, both K-major
     static constexpr uint32_t IDESC = ptx::idesc_bf16(TILE_M, BN, false);
+    static_assert(STAGES * STAGE_BYTES >= EPI_WARPS * FIX_BYTES, "the epilogue warps' end-of-work buffers live in the ring");
 };
 
 struct Params {
@@ -77,12 +99,20 @@ struct Params {
     int granule;
     int* err;
     unsigned long long timeout_ns;
-    // split-K: the k-blocks of every tile are cut into `splits` equal ranges
-    // computed by different units; each writes its fp32 partial sums to
-    // partials[split][shard][row][col] (row < M, col < N) and
-    // splitk_reduce_k sums them in split order and applies the epilogue
-    int splits;
+    // Work items: with S = n_items - dp_items split items, item i < S is
+    // part i % parts (k-blocks [kbt*j/parts, kbt*(j+1)/parts)) of tile
+    // dp_items + i / parts, and item S + t is the whole tile t < dp_items;
+    // unit u takes items u, u + units, ...  The parts come first, so the
+    // whole tiles' main loops follow them without a break.  Every part
+    // writes its fp32 sums to `partials` ([item][rank][warp][32][128]) and
+    // counts itself in (`flags`: [split tile][rank][warp] x {arrived,
+    // left}); at the end of the unit's work -- when this SM no longer
+    // streams operands, so its loads are fast -- each part reduces its own
+    // rows of the tile over all parts, in part order, and applies the
+    // epilogue.
+    int dp_items, n_items, parts;
     float* partials;
+    int* flags;
     // pre-norm variant: see TcGemm
     const float* row_scale;
     int rope_cols, rope_dh, rope_seq;
@@ -135,29 +165,37 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int group_m,
     n_blk = p.reduce ? nn : nn % p.n_blocks;
 }
 
-// One unit's work: items w = unit, unit + n_units, ... of the sequence
-// (split-major, tile-minor, so units in flight together share k ranges and
-// operand tiles); item w is tile w % n_tiles over the k-blocks of split
-// w / n_tiles.
-struct Seg {
-    int tile, split, k0, k1;
+// One piece of a unit's work: a tile and its k-block range; for a part of
+// a split tile (sk >= 0) its part index and split-item index.
+struct Item {
+    int tile, k0, k1, part, sk;
 };
-struct Sched {
-    int w, n_items, n_tiles, kbt, splits, n_units;
-    __device__ void init(const Params& p, int unit, int n_units_, int kbt_) {
+
+// The work of one unit, in order (the producer, the MMA issuer and the
+// epilogue warps each walk it with their own copy).
+struct Work {
+    int w, n_units, kbt;
+    __device__ void init(int unit, int n_units_, int kbt_) {
         w = unit;
         n_units = n_units_;
-        n_tiles = p.n_tiles;
         kbt = kbt_;
-        splits = p.splits;
-        n_items = n_tiles * splits;
     }
-    __device__ bool next(Seg& g) {
-        if (w >= n_items) return false;
-        g.tile = w % n_tiles;
-        g.split = w / n_tiles;
-        g.k0 = (int)((long long)kbt * g.split / splits);
-        g.k1 = (int)((long long)kbt * (g.split + 1) / splits);
+    __device__ bool next(const Params& p, Item& it) {
+        if (w >= p.n_items) return false;
+        const int n_split = p.n_items - p.dp_items;
+        if (w >= n_split) {
+            it.tile = w - n_split;
+            it.k0 = 0;
+            it.k1 = kbt;
+            it.part = 0;
+            it.sk = -1;
+        } else {
+            it.sk = w;
+            it.part = w % p.parts;
+            it.tile = p.dp_items + w / p.parts;
+            it.k0 = (int)((long long)kbt * it.part / p.parts);
+            it.k1 = (int)((long long)kbt * (it.part + 1) / p.parts);
+        }
         w += n_units;
         return true;
     }
@@ -165,19 +203,395 @@ struct Sched {
 
 __device__ __forceinline__ uint64_t sw128_kmajor(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
 
-// 32 consecutive bf16 of one row; `n_valid` of them inside the matrix.
-__device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32], int n_valid) {
-    if (n_valid >= 32) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+// ---- epilogue helpers ------------------------------------------------------
+// The accumulator comes out of TMEM one row per lane (32 consecutive columns
+// per lane); a 32 x 32 block goes through this warp's shared staging block
+// so that every global access of the warp covers 4 rows x 128 contiguous
+// bytes instead of 32 scattered rows.
+
+// The block is 32 rows of 128 bytes with the 16-byte chunk j of row r
+// stored at position j ^ (r % 8), so that both the row-per-lane writes and
+// the 4-rows-per-instruction reads hit 8 distinct chunk positions per phase.
+__device__ __forceinline__ void stage_put(float* stg, int lane, const float (&v)[32]) {
+    float* row = stg + lane * 32;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(row + 4 * (q ^ (lane & 7))) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+// Row 4i + lane / 8, columns 4 (lane % 8) .. + 3 of the staged block.
+__device__ __forceinline__ float4 stage_get(const float* stg, int lane, int i) {
+    const int r = 4 * i + (lane >> 3);
+    return *reinterpret_cast<const float4*>(stg + r * 32 + 4 * ((lane & 7) ^ (r & 7)));
+}
+
+// 16-byte asynchronous copy global -> shared (cached in L2 only); many can
+// be in flight per thread without holding registers.
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Pull `bytes` (a multiple of 16, 16-byte aligned) into L2 ahead of use.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint2 pack_bf16x4(float4 t) { return make_uint2(pack_bf16x2(t.x, t.y), pack_bf16x2(t.z, t.w)); }
+
+// Four consecutive residual values (row, col .. col+3), as fp32.
+__device__ __forceinline__ float4 load_res4(const Params& p, long long o) {
+    if (p.residual_f32) return *reinterpret_cast<const float4*>((const float*)p.residual + o);
+    const uint2 r = *reinterpret_cast<const uint2*>((const bf16*)p.residual + o);
+    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    return make_float4(r0.x, r0.y, r1.x, r1.y);
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+
+// Four consecutive finished outputs (row, col .. col+3), residual already
+// added: row-parallel fp32 out + optional plan-dtype copy, or a
+// column-parallel bf16 store (activation already applied).
+__device__ __forceinline__ void store4(const Params& p, int shard, int row, int col, float4 t) {
+    if (p.epi == EPI_ROW_REDUCE) {
+        const long long o = (long long)row * p.ldo + col;
+        *reinterpret_cast<float4*>((float*)p.out + o) = t;
+        if (p.out2) *reinterpret_cast<uint2*>((bf16*)p.out2 + o) = pack_bf16x4(t);
     } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < n_valid) dst[i] = __float2bfloat16_rn(v[i]);
+        *reinterpret_cast<uint2*>((bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo + col) = pack_bf16x4(t);
     }
+}
+
+// Column-parallel per-element epilogue of N consecutive columns of one row
+// (col a multiple of N): row scale, rotary embedding, GELU.
+template <int N>
+__device__ __forceinline__ void col_epilogue(const Params& p, int row, int col, float (&v)[N]) {
+    if (p.row_scale) {
+        const float rs = row < p.M ? p.row_scale[row] : 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] *= rs;
+    }
+    if (p.rope_cols > 0) apply_rope<N>(p, row, col, v);
+    if (p.epi == EPI_GELU) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = gelu_erf(v[j]);
+    }
+}
+
+// The residual rows [r0, r1) of this warp's 32, columns col0 .. col0+127,
+// pulled into L2 ahead of the epilogue that adds them (one row per lane).
+__device__ __forceinline__ void prefetch_residual(const Params& p, int lane, int row_base, int r0, int r1, int col0) {
+    if (p.epi != EPI_ROW_REDUCE || p.residual == nullptr || col0 >= p.N) return;
+    const int r = r0 + lane, grow = row_base + r;
+    if (r >= r1 || grow >= p.M) return;
+    const int es = p.residual_f32 ? 4 : 2;
+    const int ncols = min(HALF_N, p.N - col0);  // a multiple of 8
+    prefetch_l2((const char*)p.residual + ((long long)grow * p.ldo + col0) * es, (uint32_t)(ncols * es));
+}
+
+// Whole tile of a column-parallel launch: this warp's 32 rows x 128
+// columns (col0 = first column of the warp's half) from TMEM (tbase = the
+// half's first column) through the staging block; the per-element epilogue
+// runs after the transpose, 4 columns of one row per lane.
+__device__ __forceinline__ void epilogue_col(const Params& p, uint32_t tbase, float* stg, int lane, int row_base,
+                                             int shard, int col0) {
+    if (p.epi == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int g = 0; g < HALF_N / 64; ++g) {
+            float gate[32], up[32];
+            __syncwarp();
+            tmem_ld32(tbase + 64 * g, gate);
+            tmem_ld32(tbase + 64 * g + 32, up);
+            const int pc = col0 + 64 * g;  // packed column of this gate block
+            if (pc >= p.N) break;
+            float4 gv[8];
+            stage_put(stg, lane, gate);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                gv[i] = stage_get(stg, lane, i);
+            }
+            __syncwarp();
+            stage_put(stg, lane, up);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int grow = row_base + 4 * i + (lane >> 3);
+                const float4 u = stage_get(stg, lane, i);
+                const float rs = p.row_scale ? (grow < p.M ? p.row_scale[grow] : 0.f) : 1.f;
+                const float4 o = make_float4(silu(gv[i].x * rs) * (u.x * rs), silu(gv[i].y * rs) * (u.y * rs),
+                                             silu(gv[i].z * rs) * (u.z * rs), silu(gv[i].w * rs) * (u.w * rs));
+                if (grow < p.M)
+                    *reinterpret_cast<uint2*>((bf16*)p.out + shard * p.out_shard + (long long)grow * p.ldo + pc / 2 +
+                                              4 * (lane & 7)) = pack_bf16x4(o);
+            }
+            __syncwarp();
+        }
+        return;
+    }
+#pragma unroll 1
+    for (int c = 0; c < HALF_N / 32; ++c) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(tbase + 32 * c, v);
+        const int cc = col0 + 32 * c;
+        if (cc >= p.N) break;  // (warp-uniform; later chunks are further right)
+        stage_put(stg, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int grow = row_base + 4 * i + (lane >> 3), gcol = cc + 4 * (lane & 7);
+            const float4 t = stage_get(stg, lane, i);
+            float e[4] = {t.x, t.y, t.z, t.w};
+            col_epilogue<4>(p, grow, gcol, e);
+            if (grow < p.M && gcol < p.N) store4(p, shard, grow, gcol, make_float4(e[0], e[1], e[2], e[3]));
+        }
+    }
+}
+
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 r) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Whole tile of a row-parallel launch: this warp's 32 rows x 128 columns
+// plus the residual (RES 0: none, 1: bf16, 2: fp32).  Global loads take
+// about a microsecond while the tensor cores stream operands, so the
+// residual of chunk c + 1 is loaded while chunk c is stored (and the rows
+// were pulled into L2 while the MMAs ran).
+template <int RES>
+__device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, float* stg, int lane, int row_base,
+                                             int col0, float* rbuf) {
+    constexpr int NC = HALF_N / 32;
+    constexpr int L = 1;
+    if (RES != 0 && rbuf != nullptr) {
+        // the unit's last tile: the ring is idle, so the whole residual
+        // block (32 rows x 128 columns, 512-byte rows) is copied into this
+        // warp's share of it at once
+        constexpr int ES = RES == 2 ? 4 : 2;
+        const uint32_t sb = smem_u32(rbuf);
+        const int gcol = col0 + lane * 16 / ES;
+        if (lane < HALF_N * ES / 16 && gcol < p.N) {
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+                const int grow = row_base + r;
+                if (grow < p.M) cp_async16(sb + r * 512 + lane * 16, (const char*)p.residual + ((long long)grow * p.ldo + gcol) * ES);
+            }
+        }
+        cp_async_wait_all();
+        __syncwarp();
+#pragma unroll 1
+        for (int c = 0; c < NC; ++c) {
+            float v[32];
+            __syncwarp();
+            tmem_ld32(tbase + 32 * c, v);
+            const int cc = col0 + 32 * c;
+            if (cc >= p.N) break;
+            stage_put(stg, lane, v);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rr = 4 * i + (lane >> 3), lc = 32 * c + 4 * (lane & 7);
+                const int grow = row_base + rr, gcol = cc + 4 * (lane & 7);
+                float4 t = stage_get(stg, lane, i);
+                if (RES == 2) t = add4(t, *reinterpret_cast<const float4*>(rbuf + rr * HALF_N + lc));
+                if (RES == 1) t = add4(t, bf16x4_to_float4(*reinterpret_cast<const uint2*>(
+                                              reinterpret_cast<const char*>(rbuf) + rr * 512 + lc * 2)));
+                if (grow < p.M && gcol < p.N) store4(p, 0, grow, gcol, t);
+            }
+        }
+        return;
+    }
+    // one residual slot: 4 values of row 4i + lane / 8, columns c0 + 4 (lane % 8) .. + 3, as raw words
+    auto fetch = [=](int c0, int i) -> float4 {
+        const int grow = row_base + 4 * i + (lane >> 3), gcol = c0 + 4 * (lane & 7);
+        const bool ok = grow < p.M && gcol < p.N;
+        const long long o = (long long)grow * p.ldo + gcol;
+        if (RES == 1) {
+            const uint2 r = ok ? *reinterpret_cast<const uint2*>((const bf16*)p.residual + o) : make_uint2(0u, 0u);
+            return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), 0.f, 0.f);
+        }
+        return ok ? *reinterpret_cast<const float4*>((const float*)p.residual + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 rs[L][8];
+    if (RES != 0) {
+#pragma unroll
+        for (int c = 0; c < L; ++c)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rs[c][i] = fetch(col0 + 32 * c, i);
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(tbase + 32 * c, v);
+        const int cc = col0 + 32 * c;
+        if (cc >= p.N) break;  // (warp-uniform; later chunks are further right)
+        stage_put(stg, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int grow = row_base + 4 * i + (lane >> 3), gcol = cc + 4 * (lane & 7);
+            float4 t = stage_get(stg, lane, i);
+            if (RES == 1)
+                t = add4(t, bf16x4_to_float4(make_uint2(__float_as_uint(rs[c % L][i].x), __float_as_uint(rs[c % L][i].y))));
+            if (RES == 2) t = add4(t, rs[c % L][i]);
+            if (RES != 0 && c + L < NC) rs[c % L][i] = fetch(cc + 32 * L, i);  // this slot's next use
+            if (grow < p.M && gcol < p.N) store4(p, 0, grow, gcol, t);
+        }
+    }
+}
+
+// Part of a split tile: this warp's 32 rows x 128 columns of raw fp32 sums
+// to its partial block (row-major, 512-byte rows, coalesced).
+__device__ __forceinline__ void write_partial(uint32_t tbase, float* stg, int lane, float* part) {
+#pragma unroll 1
+    for (int c = 0; c < HALF_N / 32; ++c) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(tbase + 32 * c, v);
+        stage_put(stg, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            __stcg(reinterpret_cast<float4*>(part + (4 * i + (lane >> 3)) * HALF_N + 32 * c + 4 * (lane & 7)),
+                   stage_get(stg, lane, i));
+    }
+}
+
+// Bounded wait (one thread) until *cnt reaches `target`.
+__device__ __noinline__ bool wait_count(const int* cnt, int target, volatile int* abort_flag, int* err,
+                                        unsigned long long timeout_ns) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            record_error(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+// The rows [r0, r1) of this warp's 32 that this part owns, columns col0 ..
+// col0+127: the sum of all parts' partials (part order 0..parts-1), then the
+// epilogue.  `base` is part 0's block for this warp, `pstride` the distance
+// between parts, `buf` this warp's share of the idle ring: every part's
+// rows and the residual rows are copied into it at once (one memory
+// latency for the whole reduction), then summed from shared memory.
+__device__ __forceinline__ void reduce_rows(const Params& p, const float* base, long long pstride, int lane,
+                                            int row_base, int r0, int r1, int shard, int col0, float* buf) {
+    const int nr = r1 - r0;  // (parts + 1) * nr <= 48 rows of 512 bytes fit FIX_BYTES
+    const bool has_res = p.epi == EPI_ROW_REDUCE && p.residual != nullptr;
+    const int es = p.residual_f32 ? 4 : 2;
+    const uint32_t sb = smem_u32(buf);
+    const int res_off = p.parts * nr * HALF_N;  // floats: residual rows after the parts' rows
+    for (int i = 0; i < p.parts; ++i)
+        for (int j = 0; j < nr; ++j)
+            cp_async16(sb + ((i * nr + j) * HALF_N + 4 * lane) * 4, base + i * pstride + (long long)(r0 + j) * HALF_N + 4 * lane);
+    if (has_res) {
+        const int gcol = col0 + lane * 16 / es;
+        if (lane < HALF_N * es / 16 && gcol < p.N)
+            for (int j = 0; j < nr; ++j) {
+                const int grow = row_base + r0 + j;
+                if (grow < p.M)
+                    cp_async16(sb + res_off * 4 + j * 512 + lane * 16,
+                               (const char*)p.residual + ((long long)grow * p.ldo + gcol) * es);
+            }
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    if (p.epi == EPI_SWIGLU) {
+        // lane -> row j + lane / 16, gate columns 64 b + 4 (lane % 8) .. + 3 of the half (b = lane / 8 % 2)
+        // and the matching up columns 32 further
+        const int b = (lane >> 3) & 1;
+        const int gl = 64 * b + 4 * (lane & 7);
+        if (col0 + 64 * b >= p.N) return;
+        for (int j = lane >> 4; j < nr; j += 2) {
+            const int grow = row_base + r0 + j;
+            if (grow >= p.M) break;
+            float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+            for (int i = 0; i < p.parts; ++i) {
+                const float* q = buf + (i * nr + j) * HALF_N + gl;
+                g = add4(g, *reinterpret_cast<const float4*>(q));
+                u = add4(u, *reinterpret_cast<const float4*>(q + 32));
+            }
+            const float rs = p.row_scale ? p.row_scale[grow] : 1.f;
+            const float4 o = make_float4(silu(g.x * rs) * (u.x * rs), silu(g.y * rs) * (u.y * rs),
+                                         silu(g.z * rs) * (u.z * rs), silu(g.w * rs) * (u.w * rs));
+            *reinterpret_cast<uint2*>((bf16*)p.out + shard * p.out_shard + (long long)grow * p.ldo +
+                                      (col0 + 64 * b) / 2 + 4 * (lane & 7)) = pack_bf16x4(o);
+        }
+        return;
+    }
+    // lane -> columns 4 lane .. 4 lane + 3 of every row
+    const int gcol = col0 + 4 * lane;
+    if (gcol >= p.N) return;
+    for (int j = 0; j < nr; ++j) {
+        const int grow = row_base + r0 + j;
+        if (grow >= p.M) break;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < p.parts; ++i) a = add4(a, *reinterpret_cast<const float4*>(buf + (i * nr + j) * HALF_N + 4 * lane));
+        if (p.epi == EPI_ROW_REDUCE) {
+            if (has_res) {
+                const char* rrow = reinterpret_cast<const char*>(buf + res_off) + j * 512;
+                a = add4(a, es == 4 ? *reinterpret_cast<const float4*>(rrow + 16 * lane)
+                                    : bf16x4_to_float4(*reinterpret_cast<const uint2*>(rrow + 8 * lane)));
+            }
+            store4(p, shard, grow, gcol, a);
+        } else {
+            float v[4] = {a.x, a.y, a.z, a.w};
+            col_epilogue<4>(p, grow, gcol, v);
+            store4(p, shard, grow, gcol, make_float4(v[0], v[1], v[2], v[3]));
+        }
+    }
+}
+
+// The reductions of a warp's pending split parts: items w0, w0 + n_units,
+// ... (n of them).  For each, wait (bounded) until all parts of its tile
+// have counted in, reduce this part's rows of the warp's block over all
+// parts, and count out; the last part out returns the tile's counters to
+// zero.  False when a wait gave up.
+template <class C>
+__device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_units, int kbt, uint32_t rank,
+                                          int quarter, int half, int lane, volatile int* abort_flag, float* buf) {
+    const int qh = quarter * 2 + half;
+    const long long pstride = (long long)C::RANKS * EPI_WARPS * PART_FLOATS;
+    for (int k = 0; k < n; ++k) {
+        // item w0 + k * n_units is part w % parts of tile dp_items + w / parts
+        Item it;
+        it.sk = w0 + k * n_units;
+        it.part = it.sk % p.parts;
+        it.tile = p.dp_items + it.sk / p.parts;
+        int m_blk, shard, n_blk;
+        tile_coords(p, it.tile, C::GROUP_M, m_blk, shard, n_blk);
+        const int row_base = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32;
+        int* fl = p.flags + (((long long)(it.tile - p.dp_items) * C::RANKS + rank) * EPI_WARPS + qh) * 2;
+        int got = 1;
+        if (lane == 0) got = wait_count(fl, p.parts, abort_flag, p.err, p.timeout_ns) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) return false;
+        __threadfence();
+        const float* base0 = p.partials + ((long long)(it.sk - it.part) * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
+                             (long long)qh * PART_FLOATS;
+        reduce_rows(p, base0, pstride, lane, row_base, 32 * it.part / p.parts, 32 * (it.part + 1) / p.parts, shard,
+                    n_blk * BN + half * HALF_N, buf);
+        __syncwarp();
+        if (lane == 0) {
+            if (atomicAdd(fl + 1, 1) == p.parts - 1) {
+                atomicExch(fl, 0);
+                atomicExch(fl + 1, 0);
+            }
+        }
+    }
+    return true;
 }
 
 template <bool PAIR>
@@ -186,7 +600,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using C = GCfg<PAIR>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    float* stage_area = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + STG_BYTES);
     uint64_t* empty = full + C::STAGES;
     uint64_t* tmem_full = empty + C::STAGES;
     uint64_t* tmem_empty = tmem_full + 2;
@@ -195,7 +610,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // PAIR: rank in the cluster (0 issues the MMAs) and the tile stream of the pair
+    // PAIR: rank in the cluster (0 issues the MMAs) and the item stream of the pair
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const int unit = PAIR ? (int)(blockIdx.x / 2) : (int)blockIdx.x;
     const int n_units = PAIR ? (int)(gridDim.x / 2) : (int)gridDim.x;
@@ -207,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
-            mbar_init(&tmem_empty[b], PAIR ? 8 : 4);  // epilogue warps of both CTAs
+            mbar_init(&tmem_empty[b], (PAIR ? 2 : 1) * EPI_WARPS);  // epilogue warps of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -225,23 +640,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int kb_per_tile = p.reduce ? p.shards * p.k_blocks : p.k_blocks;
+    const int kbt = p.reduce ? p.shards * p.k_blocks : p.k_blocks;  // k-blocks per tile
 
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            Sched sc;
-            sc.init(p, unit, n_units, kb_per_tile);
-            Seg g;
-            while (ok && sc.next(g)) {
-                const int t = g.tile;
+            Work wk;
+            wk.init(unit, n_units, kbt);
+            Item it;
+            while (ok && wk.next(p, it)) {
                 int m_blk, shard, n_blk;
-                tile_coords(p, t, C::GROUP_M, m_blk, shard, n_blk);
+                tile_coords(p, it.tile, C::GROUP_M, m_blk, shard, n_blk);
                 const int a_row = m_blk * C::TILE_M + (int)rank * A_ROWS;
                 const int w_row = n_blk * BN + (int)rank * C::W_ROWS;
-                for (int kb = g.k0; kb < g.k1; ++kb) {
+                for (int kb = it.k0; kb < it.k1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -278,10 +692,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int i = 0;
             bool ok = true;
-            Sched sc;
-            sc.init(p, unit, n_units, kb_per_tile);
-            Seg g;
-            for (; ok && sc.next(g); ++i) {
+            Work wk;
+            wk.init(unit, n_units, kbt);
+            Item it;
+            for (; ok && wk.next(p, it); ++i) {
                 const int buf = i & 1;
                 const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
                 if (!mbar_wait(&tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
@@ -290,7 +704,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                for (int kb = g.k0; kb < g.k1; ++kb) {
+                for (int kb = it.k0; kb < it.k1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -301,7 +715,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t bdesc = sw128_kmajor(sa + C::A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {  // +32 bytes per K step inside the swizzle row
-                        const uint32_t acc = (kb > g.k0 || k > 0) ? 1u : 0u;
+                        const uint32_t acc = (kb > it.k0 || k > 0) ? 1u : 0u;
                         if constexpr (PAIR)
                             umma_f16_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), C::IDESC, acc);
                         else
@@ -331,152 +745,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t a = smem_u32(drain);
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(a, 0)) {
-                if (globaltimer() - t0 > p.timeout_ns) {
+                if (globaltimer() - t0 > drain_limit_ns(p.timeout_ns)) {
                     record_error(p.err, DEV_ERR_TIMEOUT);
                     break;
                 }
             }
         }
     } else {
-        // epilogue warps 2..5 -> TMEM lane quarters 2,3,0,1
-        const int quarter = warp & 3;
+        // epilogue warps 2..9 -> TMEM lane quarter warp % 4 (2,3,0,1,2,3,0,1)
+        // and column half (warp - 2) / 4; each warp works on its own 32 rows
+        // x 128 columns and never waits for the other epilogue warps
+        const int quarter = warp & 3, half = (warp - 2) >> 2, qh = quarter * 2 + half;
+        float* stg = stage_area + (warp - 2) * STG_FLOATS;
+        // L2 prefetch of the residual rows this warp will add for an item
+        auto prefetch_item = [&](const Item& it) {
+            int m_blk, shard, n_blk;
+            tile_coords(p, it.tile, C::GROUP_M, m_blk, shard, n_blk);
+            const int rb = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32;
+            const int r0 = it.sk >= 0 ? 32 * it.part / p.parts : 0;
+            const int r1 = it.sk >= 0 ? 32 * (it.part + 1) / p.parts : 32;
+            prefetch_residual(p, lane, rb, r0, r1, n_blk * BN + half * HALF_N);
+        };
+        // A part's partial is written (and TMEM handed back) as soon as its
+        // MMAs are done; its reduction waits for the end of the unit's work,
+        // so it neither stalls the main loops nor competes with their
+        // operand stream for this SM's loads, and no partial write ever
+        // waits for another unit.
+        int pend_w = 0, n_pend = 0;  // parts to reduce: items pend_w, pend_w + n_units, ...
+        bool ok = true;
+        // this warp's share of the ring, used only once the unit's last
+        // MMAs have completed (no copy or MMA touches the ring then)
+        float* fixbuf = reinterpret_cast<float*>(smem + (warp - 2) * FIX_BYTES);
+        Work wk;
+        wk.init(unit, n_units, kbt);
+        Item it;
         int i = 0;
-        Sched sc;
-        sc.init(p, unit, n_units, kb_per_tile);
-        Seg sg;
-        for (; sc.next(sg); ++i) {
-            const int t = sg.tile;
+        for (; wk.next(p, it); ++i) {
+            prefetch_item(it);  // (its MMAs are usually still running)
             const int buf = i & 1;
             const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
-            if (!mbar_wait_warp(&tmem_full[buf], acc_phase, abort_flag, p.err, p.timeout_ns)) break;
+            if (!mbar_wait_warp(&tmem_full[buf], acc_phase, abort_flag, p.err, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             int m_blk, shard, n_blk;
-            tile_coords(p, t, C::GROUP_M, m_blk, shard, n_blk);
-            const int row = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32 + lane;
-            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
-            const int col_base = n_blk * BN;
-            const bool row_ok = row < p.M;
-            if (p.splits > 1) {
-                // split-K: raw fp32 partial sums of this split
-                // [split][shard][row][col]; a row-parallel launch has one output "shard"
-                const int n_sh = p.reduce ? 1 : p.shards;
-                float* dst = p.partials + (((long long)sg.split * n_sh + shard) * p.M + row) * p.N;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    __syncwarp();
-                    tmem_ld32(tbase + 32 * c, v);
-                    const int col = col_base + 32 * c;
-                    if (!row_ok || col >= p.N) continue;
-                    if (col + 32 <= p.N) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + col);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            __stcg(d4 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col + j < p.N) dst[col + j] = v[j];
-                    }
-                }
-            } else if (p.epi == EPI_SWIGLU) {
-                bf16* out = (bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo;
-#pragma unroll 1
-                for (int g = 0; g < BN / 64; ++g) {
-                    float gate[32], up[32];
-                    __syncwarp();
-                    tmem_ld32(tbase + 64 * g, gate);
-                    tmem_ld32(tbase + 64 * g + 32, up);
-                    const int pc = col_base + 64 * g;  // packed column of this gate block
-                    if (row_ok && pc < p.N) {
-                        const float rs = p.row_scale ? p.row_scale[row] : 1.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) gate[j] = silu(gate[j] * rs) * (up[j] * rs);
-                        store_row_bf16(out + pc / 2, gate, 32);
-                    }
-                }
-            } else if (p.epi == EPI_ROW_REDUCE) {
-                const long long roff = (long long)row * p.ldo;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    __syncwarp();
-                    tmem_ld32(tbase + 32 * c, v);
-                    const int col = col_base + 32 * c;
-                    if (!row_ok || col >= p.N) continue;
-                    const int nv = min(32, p.N - col);
-                    if (p.residual) {
-                        if (p.residual_f32) {
-                            const float* r = (const float*)p.residual + roff + col;
-                            if (nv == 32) {
-#pragma unroll
-                                for (int q = 0; q < 8; ++q) {
-                                    const float4 x = reinterpret_cast<const float4*>(r)[q];
-                                    v[4 * q] += x.x;
-                                    v[4 * q + 1] += x.y;
-                                    v[4 * q + 2] += x.z;
-                                    v[4 * q + 3] += x.w;
-                                }
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    if (j < nv) v[j] += r[j];
-                            }
-                        } else {
-                            const bf16* r = (const bf16*)p.residual + roff + col;
-                            if (nv == 32) {
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const uint4 x = reinterpret_cast<const uint4*>(r)[q];
-                                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float2 f = __bfloat1622float2(h[e]);
-                                        v[8 * q + 2 * e] += f.x;
-                                        v[8 * q + 2 * e + 1] += f.y;
-                                    }
-                                }
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    if (j < nv) v[j] += __bfloat162float(r[j]);
-                            }
-                        }
-                    }
-                    float* o = (float*)p.out + roff + col;
-                    if (nv == 32) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            reinterpret_cast<float4*>(o)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < nv) o[j] = v[j];
-                    }
-                    if (p.out2) store_row_bf16((bf16*)p.out2 + roff + col, v, nv);
+            tile_coords(p, it.tile, C::GROUP_M, m_blk, shard, n_blk);
+            const int row_base = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + half * HALF_N);
+            const int col0 = n_blk * BN + half * HALF_N;
+            if (it.sk < 0) {
+                if (p.epi != EPI_ROW_REDUCE)
+                    epilogue_col(p, tbase, stg, lane, row_base, shard, col0);
+                else {
+                    Work peek = wk;
+                    Item nx;
+                    float* rbuf = peek.next(p, nx) ? nullptr : fixbuf;  // last item: the ring is idle
+                    if (p.residual == nullptr)
+                        epilogue_row<0>(p, tbase, stg, lane, row_base, col0, nullptr);
+                    else if (p.residual_f32)
+                        epilogue_row<2>(p, tbase, stg, lane, row_base, col0, rbuf);
+                    else
+                        epilogue_row<1>(p, tbase, stg, lane, row_base, col0, rbuf);
                 }
             } else {
-                bf16* out = (bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    __syncwarp();
-                    tmem_ld32(tbase + 32 * c, v);
-                    const int col = col_base + 32 * c;
-                    if (!row_ok || col >= p.N) continue;
-                    if (p.row_scale) {
-                        const float rs = p.row_scale[row];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= rs;
-                    }
-                    if (p.rope_cols > 0) apply_rope<32>(p, row, col, v);
-                    if (p.epi == EPI_GELU) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
-                    }
-                    store_row_bf16(out + col, v, min(32, p.N - col));
-                }
+                float* part = p.partials + ((long long)it.sk * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
+                              (long long)qh * PART_FLOATS;
+                write_partial(tbase, stg, lane, part);
             }
+            // the accumulator is in registers / memory now: hand TMEM back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -485,7 +823,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else
                     mbar_arrive(&tmem_empty[buf]);
             }
+            if (it.sk >= 0) {
+                // count this part in (its partial is complete and visible)
+                int* fl = p.flags + (((long long)(it.tile - p.dp_items) * C::RANKS + rank) * EPI_WARPS + qh) * 2;
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(fl, 1);
+                if (n_pend++ == 0) pend_w = it.sk;
+            }
         }
+        if (ok && n_pend > 0)
+            split_fixups<C>(p, pend_w, n_pend, n_units, kbt, rank, quarter, half, lane, abort_flag, fixbuf);
     }
 
     tc_fence_before();
@@ -497,82 +845,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else
             tmem_dealloc(tmem_base, TMEM_COLS);
-    }
-}
-
-// Split-K second pass: out = epilogue(sum over splits of the partial sums),
-// the splits added in order 0..S-1 (the result does not depend on which SM
-// computed which split).  Four consecutive output columns per thread.
-__global__ void __launch_bounds__(256) splitk_reduce_k(Params p) {
-    const int n_out = p.epi == EPI_SWIGLU ? p.N / 2 : p.N;  // output columns per shard
-    const int n_sh = p.reduce ? 1 : p.shards;
-    const long long quads = (long long)n_sh * p.M * n_out / 4;
-    const long long split_stride = (long long)n_sh * p.M * p.N;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < quads;
-         q += (long long)gridDim.x * blockDim.x) {
-        const long long e = q * 4;
-        const int col = (int)(e % n_out);
-        const long long rs = e / n_out;  // shard * M + row
-        const int row = (int)(rs % p.M), shard = (int)(rs / p.M);
-        const float* base = p.partials + rs * p.N;
-        float v[4];
-        if (p.epi == EPI_SWIGLU) {
-            // packed columns: gate block of 32, then the matching up block
-            const int g = (col / 32) * 64 + col % 32;
-            float4 ga = __ldcg(reinterpret_cast<const float4*>(base + g));
-            float4 ua = __ldcg(reinterpret_cast<const float4*>(base + g + 32));
-            for (int sp = 1; sp < p.splits; ++sp) {
-                const float4 gb = __ldcg(reinterpret_cast<const float4*>(base + sp * split_stride + g));
-                const float4 ub = __ldcg(reinterpret_cast<const float4*>(base + sp * split_stride + g + 32));
-                ga.x += gb.x; ga.y += gb.y; ga.z += gb.z; ga.w += gb.w;
-                ua.x += ub.x; ua.y += ub.y; ua.z += ub.z; ua.w += ub.w;
-            }
-            const float sc = p.row_scale ? p.row_scale[row] : 1.f;
-            v[0] = silu(ga.x * sc) * (ua.x * sc);
-            v[1] = silu(ga.y * sc) * (ua.y * sc);
-            v[2] = silu(ga.z * sc) * (ua.z * sc);
-            v[3] = silu(ga.w * sc) * (ua.w * sc);
-        } else {
-            float4 a = __ldcg(reinterpret_cast<const float4*>(base + col));
-            for (int sp = 1; sp < p.splits; ++sp) {
-                const float4 b = __ldcg(reinterpret_cast<const float4*>(base + sp * split_stride + col));
-                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-            }
-            v[0] = a.x;
-            v[1] = a.y;
-            v[2] = a.z;
-            v[3] = a.w;
-            if (p.row_scale) {
-                const float sc = p.row_scale[row];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) v[j] *= sc;
-            }
-            if (p.rope_cols > 0) apply_rope<4>(p, row, col, v);
-            if (p.epi == EPI_GELU) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) v[j] = gelu_erf(v[j]);
-            }
-        }
-        if (p.epi == EPI_ROW_REDUCE) {
-            const long long o = (long long)row * p.ldo + col;
-            if (p.residual) {
-                if (p.residual_f32) {
-                    const float4 r = *reinterpret_cast<const float4*>((const float*)p.residual + o);
-                    v[0] += r.x; v[1] += r.y; v[2] += r.z; v[3] += r.w;
-                } else {
-                    const uint2 r = *reinterpret_cast<const uint2*>((const bf16*)p.residual + o);
-                    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
-                    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
-                    v[0] += r0.x; v[1] += r0.y; v[2] += r1.x; v[3] += r1.y;
-                }
-            }
-            *reinterpret_cast<float4*>((float*)p.out + o) = make_float4(v[0], v[1], v[2], v[3]);
-            if (p.out2)
-                *reinterpret_cast<uint2*>((bf16*)p.out2 + o) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-        } else {
-            bf16* o = (bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo + col;
-            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-        }
     }
 }
 
@@ -675,8 +947,56 @@ cudaError_t set_smem_attr() {
     return cudaSuccess;
 }
 
-// Largest split factor; a split keeps at least this many k-blocks.
-constexpr int SPLITK_MAX = 16, SPLITK_MIN_KB = 4;
+// Split tiles: at most this many parts per tile, at least this many
+// k-blocks per part, at most this many split items per unit (the partials'
+// scratch); writing a part's 128 KB partial per SM takes about as long as
+// SPLIT_EPI_KB k-blocks of MMAs, so shorter parts leave the epilogue
+// behind; the reductions at the end of the launch are left exposed
+// (SPLIT_COST_KB) and move every partial twice (written, read back):
+// about SPLIT_MB_PER_KB MB of that traffic over the whole GPU costs one
+// k-block of time (a k-block of a tile takes ~0.4 us; ~4 TB/s for the mixed
+// L2 / HBM traffic of the reductions).
+constexpr int SPLIT_MAX_PARTS = 16, SPLIT_MIN_KB = 4, SPLIT_MAX_ROUNDS = SPLIT_ROUNDS_MAX, SPLIT_EPI_KB = 6,
+              SPLIT_COST_KB = 2;
+constexpr double SPLIT_MB_PER_KB = 1.6;
+constexpr size_t FLAG_BYTES = 16384;  // [split tile][rank][epilogue warp][2] ints; split tiles < units <= SMs
+
+struct Decomp {
+    int dp, parts, n_items, units;
+    size_t scratch;  // bytes of scratch touched
+};
+
+// Work decomposition over `units` co-resident units (SM pairs or SMs) for
+// T tiles of kbt k-blocks: the tiles that fill whole rounds run whole; the
+// remaining tiles are cut into equal k-parts (run first) so that the units
+// end evenly loaded.  The makespan (in k-blocks per unit) decides.
+Decomp choose_decomp(int T, int kbt, int units, int ranks, size_t scratch_bytes) {
+    Decomp d{T, 1, T, T < units ? T : units, 0};
+    long long best = (long long)((T + units - 1) / units) * kbt;
+    if (scratch_bytes <= FLAG_BYTES) return d;
+    const int full = T / units, rem = T - full * units;
+    if (rem == 0 || (size_t)rem * ranks * EPI_WARPS * 2 * sizeof(int) > FLAG_BYTES) return d;
+    for (int parts = 2; parts <= SPLIT_MAX_PARTS && kbt / parts >= SPLIT_MIN_KB; ++parts) {
+        const long long items = (long long)rem * parts;
+        if (items > (long long)SPLIT_MAX_ROUNDS * units) break;
+        const size_t need = FLAG_BYTES + (size_t)items * ranks * A_ROWS * BN * sizeof(float);
+        if (need > scratch_bytes) break;
+        const long long rounds = (items + units - 1) / units;
+        const long long per_item = (kbt + parts - 1) / parts;
+        const double traffic_mb = 2.0 * (double)items * ranks * A_ROWS * BN * sizeof(float) / 1e6;
+        const long long span = (long long)full * kbt + rounds * (per_item > SPLIT_EPI_KB ? per_item : SPLIT_EPI_KB) +
+                               SPLIT_COST_KB + (long long)(traffic_mb / SPLIT_MB_PER_KB);
+        if (span < best) {
+            best = span;
+            d.dp = full * units;
+            d.parts = parts;
+            d.n_items = (int)(d.dp + items);
+            d.units = units;
+            d.scratch = need;
+        }
+    }
+    return d;
+}
 
 template <bool PAIR>
 cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch, size_t scratch_bytes,
@@ -709,28 +1029,22 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     p.residual_f32 = g.residual_f32;
     p.granule = g.granule;
     p.err = dev_err;
-    p.timeout_ns = DEFAULT_TIMEOUT_NS;
+    p.timeout_ns = wait_timeout_ns();
     p.row_scale = g.row_scale;
     p.rope_cols = g.rope_cols;
     p.rope_dh = g.rope_dh;
     p.rope_seq = g.rope_seq > 0 ? g.rope_seq : 1;
     p.rope_cs = g.rope_cs;
-    p.splits = 1;
-    // split-K when whole tiles would leave at least half of the units idle
-    if (scratch && 2 * p.n_tiles <= slots) {
-        const int kbt = (g.reduce ? g.shards : 1) * p.k_blocks;
-        int S = slots / p.n_tiles;
-        if (S > SPLITK_MAX) S = SPLITK_MAX;
-        if (S > kbt / SPLITK_MIN_KB) S = kbt / SPLITK_MIN_KB;
-        const size_t need = (size_t)S * (g.reduce ? 1 : g.shards) * g.M * g.N * sizeof(float);
-        if (S >= 2 && need <= scratch_bytes) {
-            p.splits = S;
-            p.partials = static_cast<float*>(scratch);
-        }
+    const int kbt = (g.reduce ? g.shards : 1) * p.k_blocks;
+    const Decomp d = choose_decomp(p.n_tiles, kbt, slots, C::RANKS, scratch ? scratch_bytes : 0);
+    p.dp_items = d.dp;
+    p.parts = d.parts;
+    p.n_items = d.n_items;
+    if (d.parts > 1) {
+        p.flags = static_cast<int*>(scratch);
+        p.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + FLAG_BYTES);
     }
-    const int items = p.n_tiles * p.splits;
-    const int units = items < slots ? items : slots;
-    cudaError_t e = cudaSuccess;
+    const int units = d.units;
     if constexpr (PAIR) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -744,28 +1058,41 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, tmA, tmW, p);
+        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, tmA, tmW, p);
     } else {
         tc_gemm_kernel<false><<<units, NUM_THREADS, C::SMEM, st>>>(tmA, tmW, p);
-        e = cudaGetLastError();
+        return cudaGetLastError();
     }
-    if (e != cudaSuccess || p.splits == 1) return e;
-    const long long quads = (long long)(g.reduce ? 1 : g.shards) * g.M * (g.epi == EPI_SWIGLU ? g.N / 2 : g.N) / 4;
-    long long blocks = (quads + 255) / 256;
-    if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
-    splitk_reduce_k<<<(unsigned)blocks, 256, 0, st>>>(p);
-    return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t tc_gemm_scratch_bytes() {
-    // S * tiles <= units, so the partials never exceed one 128 x 256 fp32 tile per SM
-    return (size_t)sm_count() * A_ROWS * BN * sizeof(float);
+    // split items <= SPLIT_MAX_ROUNDS per unit, and ranks x units <= SMs, so
+    // the partials never exceed SPLIT_MAX_ROUNDS 128 x 256 fp32 blocks per SM
+    return FLAG_BYTES + (size_t)SPLIT_MAX_ROUNDS * sm_count() * A_ROWS * BN * sizeof(float);
+}
+
+TcSchedule tc_gemm_schedule(const TcGemm& g, size_t scratch_bytes, int sms, int slots) {
+    TcSchedule r{};
+    r.paired = g.M > A_ROWS && slots > 0;
+    const int tile_m = r.paired ? 256 : 128;
+    const int m_blocks = (g.M + tile_m - 1) / tile_m, n_blocks = (g.N + BN - 1) / BN;
+    r.tiles = m_blocks * n_blocks * (g.reduce ? 1 : g.shards);
+    r.kbt = (g.reduce ? g.shards : 1) * ((g.K + BK - 1) / BK);
+    const int ranks = r.paired ? 2 : 1;
+    const Decomp d = choose_decomp(r.tiles, r.kbt, r.paired ? slots : sms, ranks, scratch_bytes);
+    r.units = d.units;
+    r.scratch_touched = d.scratch;
+    r.whole = d.dp;
+    r.parts = d.parts;
+    r.items = d.n_items;
+    return r;
 }
 
 cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st) {
     if (g.epi == EPI_SWIGLU && (g.granule != 32 || g.N % 64 != 0)) return cudaErrorNotSupported;
+    if (g.N % 8 != 0 || g.ldo % 8 != 0) return cudaErrorNotSupported;  // 4- and 8-wide vector stores
     cudaError_t e = set_smem_attr<false>();
     if (e == cudaSuccess) e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;

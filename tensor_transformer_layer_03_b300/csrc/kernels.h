@@ -85,10 +85,24 @@ struct TcGemm {
     const float2* rope_cs;
 };
 bool tc_gemm_supported(int M, int N, int K);
-// scratch (nullable): stream-K partials and flags, at least
-// tc_gemm_scratch_bytes() to be used; without it every launch runs whole tiles
+// scratch (nullable): the split tiles' counters (zero-filled before first
+// use; every launch that completes leaves them zero) and fp32 partial sums;
+// at most tc_gemm_scratch_bytes() is touched.  Without scratch every launch
+// runs whole tiles only.
 size_t tc_gemm_scratch_bytes();
 cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st);
+// Host-only description of a tc_gemm launch on a GPU with `sms` SMs of which
+// `pair_slots` SM pairs can be co-resident (0: no paired launches).
+struct TcSchedule {
+    int paired;            // 2-SM tiles (256 rows) or single-SM tiles (128 rows)
+    int tiles, kbt;        // output tiles, k-blocks per tile
+    int whole, parts;      // tiles run whole; parts per remaining (split) tile
+    int items, units;      // work items (split parts first, then whole tiles), units (SM pairs or SMs)
+    size_t scratch_touched;  // bytes of scratch the launch reads or writes
+};
+TcSchedule tc_gemm_schedule(const TcGemm& g, size_t scratch_bytes, int sms, int pair_slots);
+// Limit of every bounded wait in the tensor-core kernels (ns).
+unsigned long long wait_timeout_ns();
 
 // ---- small-M weight streaming (gemv.cu): same arguments as the GEMM ---------
 typedef TcGemm GemvArgs;

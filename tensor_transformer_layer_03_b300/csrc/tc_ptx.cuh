@@ -45,6 +45,15 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
+// The wait for a kernel's own tensor-core work to drain before TMEM is
+// freed never gives up sooner than this, whatever the configured wait limit:
+// MMAs that were issued always complete, and freeing TMEM under them is not
+// allowed.
+constexpr unsigned long long DRAIN_MIN_NS = 200000000ull;  // 200 ms
+__host__ __device__ constexpr unsigned long long drain_limit_ns(unsigned long long timeout_ns) {
+    return timeout_ns > DRAIN_MIN_NS ? timeout_ns : DRAIN_MIN_NS;
+}
+
 // Slow path of mbar_wait: poll with a deadline.
 __device__ __noinline__ inline bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                    int* err, unsigned long long timeout_ns) {

@@ -25,6 +25,9 @@ namespace {
 
 thread_local char g_last_cuda_error[256] = "";
 
+constexpr unsigned long long DEFAULT_WAIT_TIMEOUT_NS = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_timeout_ns{DEFAULT_WAIT_TIMEOUT_NS};
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool misaligned(const void* p) { return tpk::misaligned16(p); }
@@ -130,6 +133,88 @@ struct ColumnExtras {
 static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M, const void* packed,
                                     void* out_shards, void* scratch, size_t scratch_bytes, const ColumnExtras& ex,
                                     cudaStream_t st);
+
+unsigned long long tpk::wait_timeout_ns() { return g_wait_timeout_ns.load(); }
+
+// The linear launches: argument records of the tensor-core / weight-streaming
+// kernels, and which kernel a call runs (shared by the calls and by
+// tp_linear_schedule, so the schedule query reports what the calls do).
+enum LinearKernel { LK_TC = 0, LK_GEMV_MMA = 1, LK_GEMV = 2, LK_SIMT = 3 };
+
+static tpk::TcGemm column_gemm(const tp_plan_s* p, int which, const void* x, int M, const void* packed,
+                               void* out_shards, const ColumnExtras& ex) {
+    const bool qkv = which == TP_QKV;
+    const int N = qkv ? 3 * p->hl * p->dh : p->up_rows;  // W rows per shard
+    const int n_out = qkv ? N : p->fl;                     // output columns per shard
+    tpk::TcGemm g{};
+    g.epi = qkv ? tpk::EPI_STORE : (p->act == TP_ACT_SWIGLU ? tpk::EPI_SWIGLU : tpk::EPI_GELU);
+    g.A = x;
+    g.a_shard = 0;
+    g.lda = p->d;
+    g.W = ptr_at(packed, qkv ? p->off_qkv : p->off_up);
+    g.w_shard = (long long)N * p->d;
+    g.M = M;
+    g.N = N;
+    g.K = p->d;
+    g.shards = p->tp;
+    g.reduce = 0;
+    g.out = out_shards;
+    g.out_shard = (long long)M * n_out;
+    g.ldo = n_out;
+    g.granule = p->granule;
+    g.row_scale = ex.row_scale;
+    if (ex.rope_cs) {
+        g.rope_cols = 2 * p->hl * p->dh;  // the Q and K heads of each shard's [Q | K | V] row
+        g.rope_dh = p->dh;
+        g.rope_seq = ex.rope_seq;
+        g.rope_cs = ex.rope_cs;
+    }
+    return g;
+}
+
+static tpk::TcGemm row_gemm(const tp_plan_s* p, int which, const void* in_shards, int M, const void* packed,
+                            const void* residual, void* out_f32, void* out_act) {
+    const bool attn = which == TP_ATTN_OUT;
+    const int ks = attn ? p->hl * p->dh : p->fl;
+    tpk::TcGemm g{};
+    g.epi = tpk::EPI_ROW_REDUCE;
+    g.A = in_shards;
+    g.a_shard = (long long)M * ks;
+    g.lda = ks;
+    g.W = ptr_at(packed, attn ? p->off_o : p->off_down);
+    g.w_shard = (long long)p->d * ks;
+    g.M = M;
+    g.N = p->d;
+    g.K = ks;
+    g.shards = p->tp;
+    g.reduce = 1;
+    g.out = out_f32;
+    g.ldo = p->d;
+    g.out2 = out_act;
+    g.residual = residual;
+    g.residual_f32 = attn ? (p->dtype == TP_FP32) : 1;
+    return g;
+}
+
+static LinearKernel pick_linear(const tp_plan_s* p, const tpk::TcGemm& g) {
+    if (p->dtype != TP_BF16) return LK_SIMT;
+    const int M = g.M;
+    if (M >= 2 && M <= tpk::GEMV_MAX_M && tpk::gemv_mma_supported(g)) return LK_GEMV_MMA;
+    const bool tc_ok = tpk::tc_gemm_supported(M, g.N, g.K) && (g.epi != tpk::EPI_SWIGLU || g.granule == 32);
+    if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok)) return LK_GEMV;
+    return tc_ok ? LK_TC : LK_SIMT;
+}
+
+// Launch the bf16 linear `g` on the kernel pick_linear chose.
+static tp_status run_linear(LinearKernel k, const tpk::TcGemm& g, void* scratch, size_t scratch_bytes,
+                            cudaStream_t st) {
+    switch (k) {
+        case LK_GEMV_MMA: return cuda_status(tpk::gemv_mma(g, st));
+        case LK_GEMV: return cuda_status(tpk::gemv(g, device_error_word(), st));
+        case LK_TC: return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
+        default: return TP_ERR_UNSUPPORTED;
+    }
+}
 
 tp_status tpk::status_from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return TP_OK;
@@ -378,34 +463,9 @@ static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M
     const void* W = ptr_at(packed, qkv ? p->off_qkv : p->off_up);
     const int epi = qkv ? tpk::EPI_STORE : (p->act == TP_ACT_SWIGLU ? tpk::EPI_SWIGLU : tpk::EPI_GELU);
     if (p->dtype == TP_BF16) {
-        tpk::TcGemm g{};
-        g.epi = epi;
-        g.A = x;
-        g.a_shard = 0;
-        g.lda = p->d;
-        g.W = W;
-        g.w_shard = (long long)N * p->d;
-        g.M = M;
-        g.N = N;
-        g.K = p->d;
-        g.shards = p->tp;
-        g.reduce = 0;
-        g.out = out_shards;
-        g.out_shard = (long long)M * n_out;
-        g.ldo = n_out;
-        g.granule = p->granule;
-        g.row_scale = ex.row_scale;
-        if (ex.rope_cs) {
-            g.rope_cols = 2 * p->hl * p->dh;  // the Q and K heads of each shard's [Q | K | V] row
-            g.rope_dh = p->dh;
-            g.rope_seq = ex.rope_seq;
-            g.rope_cs = ex.rope_cs;
-        }
-        if (M >= 2 && M <= tpk::GEMV_MAX_M && tpk::gemv_mma_supported(g)) return cuda_status(tpk::gemv_mma(g, st));
-        const bool tc_ok = tpk::tc_gemm_supported(M, N, p->d) && (epi != tpk::EPI_SWIGLU || p->granule == 32);
-        if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok))
-            return cuda_status(tpk::gemv(g, device_error_word(), st));
-        if (tc_ok) return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
+        const tpk::TcGemm g = column_gemm(p, which, x, M, packed, out_shards, ex);
+        const LinearKernel k = pick_linear(p, g);
+        if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st);
     }
     if (ex.row_scale) return TP_ERR_UNSUPPORTED;  // (plan creation rules this out for pre-norm plans)
     tpk::SimtGemm g{};
@@ -446,28 +506,9 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
     const void* W = ptr_at(packed, attn ? p->off_o : p->off_down);
     const int res_f32 = attn ? (p->dtype == TP_FP32) : 1;
     if (p->dtype == TP_BF16) {
-        tpk::TcGemm g{};
-        g.epi = tpk::EPI_ROW_REDUCE;
-        g.A = in_shards;
-        g.a_shard = (long long)M * ks;
-        g.lda = ks;
-        g.W = W;
-        g.w_shard = (long long)p->d * ks;
-        g.M = M;
-        g.N = p->d;
-        g.K = ks;
-        g.shards = p->tp;
-        g.reduce = 1;
-        g.out = out_f32;
-        g.ldo = p->d;
-        g.out2 = out_act;
-        g.residual = residual;
-        g.residual_f32 = res_f32;
-        if (M >= 2 && M <= tpk::GEMV_MAX_M && tpk::gemv_mma_supported(g)) return cuda_status(tpk::gemv_mma(g, st));
-        const bool tc_ok = tpk::tc_gemm_supported(M, p->d, ks);
-        if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok))
-            return cuda_status(tpk::gemv(g, device_error_word(), st));
-        if (tc_ok) return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
+        const tpk::TcGemm g = row_gemm(p, which, in_shards, M, packed, residual, out_f32, out_act);
+        const LinearKernel k = pick_linear(p, g);
+        if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st);
     }
     tpk::SimtGemm g{};
     g.epi = tpk::EPI_ROW_REDUCE;
@@ -592,6 +633,36 @@ tp_status tp_stack_forward(tp_plan_t p, int n_layers, const void* const* packed_
                                v_caches ? v_caches[l] : nullptr, cache_cap, cache_pos, packed_layers[l], workspace, w,
                                out_f32, copy, stream);
         if (s != TP_OK) return s;
+    }
+    return TP_OK;
+}
+
+void tp_set_wait_timeout_ns(unsigned long long ns) {
+    g_wait_timeout_ns.store(ns ? ns : DEFAULT_WAIT_TIMEOUT_NS);
+}
+
+tp_status tp_linear_schedule(tp_plan_t p, int row, int which, int M, size_t scratch_bytes, int sms, int pair_slots,
+                             tp_linear_schedule_t* out) {
+    if (!p || !out) return TP_ERR_NULL_ARG;
+    if (M <= 0 || sms <= 0 || pair_slots < 0 || (row != 0 && row != 1) || (which != 0 && which != 1))
+        return TP_ERR_INVALID_DIM;
+    static const int zero_rows[1] = {0};
+    const void* fake = zero_rows;  // never dereferenced: only the shapes matter here
+    const tpk::TcGemm g = row ? row_gemm(p, which, fake, M, fake, nullptr, nullptr, nullptr)
+                              : column_gemm(p, which, fake, M, fake, nullptr, ColumnExtras());
+    *out = tp_linear_schedule_t{};
+    const LinearKernel k = pick_linear(p, g);
+    out->kernel = (int)k;
+    if (k == LK_TC) {
+        const tpk::TcSchedule r = tpk::tc_gemm_schedule(g, scratch_bytes, sms, pair_slots);
+        out->paired = r.paired;
+        out->tiles = r.tiles;
+        out->k_blocks_per_tile = r.kbt;
+        out->whole_tiles = r.whole;
+        out->parts = r.parts;
+        out->items = r.items;
+        out->units = r.units;
+        out->scratch_bytes_touched = r.scratch_touched;
     }
     return TP_OK;
 }

@@ -57,7 +57,15 @@ EXPORTS = {
     "tp_stack_forward": (_i, [_p, _i, ctypes.POINTER(_p), _p, _i, _i, _i, ctypes.POINTER(_p), ctypes.POINTER(_p),
                               _i, _i, _p, _sz, _p, _p]),
     "tp_sync_status": (_i, [_p]),
+    "tp_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+    "tp_linear_schedule": (_i, [_p, _i, _i, _i, _sz, _i, _i, _p]),
 }
+
+
+class LinearSchedule(ctypes.Structure):
+    """tp_linear_schedule_t."""
+    _fields_ = [("kernel", _i), ("paired", _i), ("tiles", _i), ("k_blocks_per_tile", _i), ("whole_tiles", _i),
+                ("parts", _i), ("items", _i), ("units", _i), ("scratch_bytes_touched", _sz)]
 for _name, (_res, _args) in EXPORTS.items():
     _f = getattr(lib, _name)
     _f.restype = _res
@@ -153,6 +161,13 @@ class Plan:
         check(tp_shard_weights(self.handle, _ptr(w["Wq"]), _ptr(w["Wk"]), _ptr(w["Wv"]), _ptr(w["Wo"]),
                                _ptr(first), _ptr(up), _ptr(w["Wd"]), _ptr(packed), _stream(stream)),
               "tp_shard_weights")
+
+    def linear_schedule(self, row, which, M, scratch_bytes, sms=148, pair_slots=74):
+        """Host-only: how the linear would run (tp_linear_schedule)."""
+        out = LinearSchedule()
+        check(tp_linear_schedule(self.handle, int(row), which, M, scratch_bytes, sms, pair_slots,
+                                 ctypes.cast(ctypes.byref(out), ctypes.c_void_p)), "tp_linear_schedule")
+        return out
 
     def linear_scratch_bytes(self, M):
         b = _sz()

@@ -51,9 +51,19 @@ def _packed(tp_mod, plan, shape, dtype, seed):
 
 
 def _scratch(plan, M, use):
-    """Stream-K scratch for the linears (None: whole-tile schedule)."""
+    """Split-tile scratch for the linears, zero-filled as the ABI requires
+    before first use (None: whole tiles only)."""
     n = plan.linear_scratch_bytes(M) if use else 0
-    return torch.empty(n, dtype=torch.uint8, device=DEV) if n else None
+    return torch.zeros(n, dtype=torch.uint8, device=DEV) if n else None
+
+
+def _again_equal(call, out, what):
+    """A second call on the same (already used) scratch gives the same bits:
+    the split-tile counters are back at zero after every call."""
+    first = out.clone()
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first), f"{what}: second call on the same scratch differs"
 
 
 def _check(got, ref, dtype, what):
@@ -71,8 +81,12 @@ def test_column_qkv(tp, d, H, f, deg, M, dtype, sk):
     w, packed = _packed(tp, plan, shape, dtype, 1)
     x = I.make_matrix(M, d, dtype, _gen(2))
     out = torch.empty(deg, M, 3 * d // deg, dtype=I.torch_dtype(dtype), device=DEV)
-    plan.column_linear(tp.TP_QKV, x.to(DEV), M, packed, out, scratch=_scratch(plan, M, sk))
+    scr = _scratch(plan, M, sk)
+    xd = x.to(DEV)
+    plan.column_linear(tp.TP_QKV, xd, M, packed, out, scratch=scr)
     plan.sync_status()
+    if scr is not None:
+        _again_equal(lambda: plan.column_linear(tp.TP_QKV, xd, M, packed, out, scratch=scr), out, "QKV")
     ref = qkv_shards(o.linear(x, w["Wq"]), o.linear(x, w["Wk"]), o.linear(x, w["Wv"]), deg, H)
     if dtype == "bf16":
         ref = o.round_bf16(ref)
@@ -89,8 +103,12 @@ def test_column_ffn_up(tp, d, H, f, deg, M, dtype, act, sk):
     w, packed = _packed(tp, plan, shape, dtype, 3)
     h = I.make_matrix(M, d, dtype, _gen(4))
     out = torch.empty(deg, M, f // deg, dtype=I.torch_dtype(dtype), device=DEV)
-    plan.column_linear(tp.TP_FFN_UP, h.to(DEV), M, packed, out, scratch=_scratch(plan, M, sk))
+    scr = _scratch(plan, M, sk)
+    hd = h.to(DEV)
+    plan.column_linear(tp.TP_FFN_UP, hd, M, packed, out, scratch=scr)
     plan.sync_status()
+    if scr is not None:
+        _again_equal(lambda: plan.column_linear(tp.TP_FFN_UP, hd, M, packed, out, scratch=scr), out, "FFN-up")
     if act == "swiglu":
         u = o.silu(o.linear(h, w["Wg"])) * o.linear(h, w["Wu"])
     else:
@@ -123,8 +141,12 @@ def test_row_reduce(tp, d, H, f, deg, M, dtype, which, sk):
     out = torch.empty(M, d, dtype=torch.float32, device=DEV)
     out_act = torch.empty(M, d, dtype=I.torch_dtype(dtype), device=DEV)
     scr = _scratch(plan, M, sk)
-    plan.row_linear_reduce(code, inp.to(DEV), M, packed, res.to(DEV), out, out_act, scratch=scr)
+    ind, resd = inp.to(DEV), res.to(DEV)
+    plan.row_linear_reduce(code, ind, M, packed, resd, out, out_act, scratch=scr)
     plan.sync_status()
+    if scr is not None:
+        _again_equal(lambda: plan.row_linear_reduce(code, ind, M, packed, resd, out, out_act, scratch=scr), out,
+                     "row reduce")
     a_full = unshard_cols(inp)
     ref = np64(res) + o.all_reduce_sum(o.row_parallel_partials(a_full, W, deg))
     # fp32 output: accumulation-order noise only.  fp32 plans: <= 1e-5; bf16
@@ -221,3 +243,57 @@ def test_attention_with_cache(tp, d, H, deg, B, T, pos, cap, dtype):
         assert np.array_equal(kn[b, :, pos:pos + T], new)
         assert np.array_equal(kn[b, :, :pos], np64(kc[b, :, :pos]))
         assert np.array_equal(kn[b, :, pos + T:], np64(kc[b, :, pos + T:]), equal_nan=True)
+
+
+@pytest.mark.parametrize("deg,M", [(4, 2048), (2, 128), (4, 512)])
+def test_linears_split_tiles_7b(tp, deg, M):
+    """The four linears of the 7B-shaped block at prompt sizes whose tiles
+    do not fill the SMs evenly (the last round's tiles cut into parts,
+    checked against the host-side schedule query), compared with the oracle
+    on sampled rows (rows are independent)."""
+    d, H, f = 4096, 32, 11008
+    plan = _plan(tp, d, H, f, deg)
+    shape = I.BlockShape(d, H, f, "swiglu")
+    w, packed = _packed(tp, plan, shape, "bf16", 7)
+    g = _gen(8)
+    scr = _scratch(plan, M, True)
+    nscr = scr.numel()
+    rows = sorted(r for r in set([0, 1, 127, 128, M // 2, M - 2, M - 1] + torch.randint(0, M, (9,), generator=g).tolist())
+                  if r < M)
+    # column QKV and FFN-up
+    x = I.make_matrix(M, d, "bf16", g)
+    for which, name in ((tp.TP_QKV, "QKV"), (tp.TP_FFN_UP, "FFN-up")):
+        sch = plan.linear_schedule(0, which, M, nscr)
+        n_out = 3 * d // deg if which == tp.TP_QKV else f // deg
+        out = torch.empty(deg, M, n_out, dtype=torch.bfloat16, device=DEV)
+        plan.column_linear(which, x.to(DEV), M, packed, out, scratch=scr)
+        plan.sync_status()
+        xs = x[rows]
+        if which == tp.TP_QKV:
+            ref = qkv_shards(o.linear(xs, w["Wq"]), o.linear(xs, w["Wk"]), o.linear(xs, w["Wv"]), deg, H)
+        else:
+            ref = col_shards(o.silu(o.linear(xs, w["Wg"])) * o.linear(xs, w["Wu"]), deg)
+        assert_close_bf16(out[:, rows].cpu(), o.round_bf16(ref),
+                          f"{name} M={M} tp{deg} (kernel {sch.kernel}, parts {sch.parts}, whole {sch.whole_tiles})")
+    # row-parallel O and FFN-down with residual and act copy
+    for which, name, ks, W, res_dtype in ((tp.TP_ATTN_OUT, "O", d // deg, w["Wo"], "bf16"),
+                                          (tp.TP_FFN_DOWN, "FFN-down", f // deg, w["Wd"], "fp32")):
+        sch = plan.linear_schedule(1, which, M, nscr)
+        inp = torch.stack([I.make_matrix(M, ks, "bf16", g) for _ in range(deg)])
+        res = I.make_matrix(M, d, res_dtype, g)
+        out = torch.empty(M, d, dtype=torch.float32, device=DEV)
+        out_act = torch.empty(M, d, dtype=torch.bfloat16, device=DEV)
+        plan.row_linear_reduce(which, inp.to(DEV), M, packed, res.to(DEV), out, out_act, scratch=scr)
+        plan.sync_status()
+        ref = np64(res[rows]) + o.all_reduce_sum(o.row_parallel_partials(unshard_cols(inp[:, rows]), W, deg))
+        nw = float(np.max(np.abs(np64(out[rows]) - ref)) / np.max(np.abs(ref)))
+        assert nw <= 1e-4, (name, M, deg, nw, sch.parts)
+        assert_close_bf16(out_act[rows].cpu(), o.round_bf16(ref), f"{name} act copy M={M} tp{deg}")
+    # the headline prompt's QKV runs whole tiles and cut parts; the
+    # 128-token prompt (fewer tiles than SMs) cuts every O tile
+    if M == 2048:
+        s = plan.linear_schedule(0, tp.TP_QKV, M, nscr)
+        assert s.kernel == 0 and s.paired and s.parts > 1 and s.whole_tiles > 0
+    if M == 128:
+        s = plan.linear_schedule(1, tp.TP_ATTN_OUT, M, nscr)
+        assert s.kernel == 0 and not s.paired and s.parts > 1 and s.whole_tiles == 0
