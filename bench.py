@@ -411,19 +411,29 @@ def run_ours(args):
     stages = ["column_qkv", "attention", "row_o_reduce", "column_ffn_up_swiglu", "row_ffn_down_reduce"]
 
     def step(ev):
+        """The five launches of one block step.  `ev` holds 2 events (the
+        step's start and end: the launches run back to back, each one's
+        set-up overlapping the previous one's tail) or 6 (one between every
+        two launches, for the per-stage times; an event between two launches
+        keeps the second from starting early)."""
+        per_stage = len(ev) == 6
         ev[0].record(stream)
         plan.column_linear(tpb.TP_QKV, x, M, blk.packed, qkv, stream, scratch=gscr)
-        ev[1].record(stream)
+        if per_stage:
+            ev[1].record(stream)
         plan.attention_heads(qkv, B, T, wl.causal, None, None, 0, 0, att, None, stream)
-        ev[2].record(stream)
+        if per_stage:
+            ev[2].record(stream)
         plan.row_linear_reduce(tpb.TP_ATTN_OUT, att, M, blk.packed, x, hf, ha, stream, scratch=gscr)
-        ev[3].record(stream)
+        if per_stage:
+            ev[3].record(stream)
         plan.column_linear(tpb.TP_FFN_UP, ha, M, blk.packed, u, stream, scratch=gscr)
-        ev[4].record(stream)
+        if per_stage:
+            ev[4].record(stream)
         plan.row_linear_reduce(tpb.TP_FFN_DOWN, u, M, blk.packed, hf, y, None, stream, scratch=gscr)
-        ev[5].record(stream)
+        ev[-1].record(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps + args.warmup)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps + args.warmup)]
     clk = ClockSampler(local).start()
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -446,10 +456,17 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         if pg is not None:
             pg.barrier()
+        # per-stage times: the same steps again with an event between every
+        # two launches (diagnostic; the headline uses the whole-step events)
+        n_stage = min(args.steps, 200)
+        sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_stage)]
+        for i in range(n_stage):
+            flush.fill_(i & 0xFF)
+            step(sevs[i])
+        stream.synchronize()
     plan.sync_status(stream)
-    per_stage = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.warmup, args.warmup + args.steps)]
-                 for j in range(5)]
-    step_ms = [sum(per_stage[j][k] for j in range(5)) for k in range(args.steps)]
+    per_stage = [[sevs[i][j].elapsed_time(sevs[i][j + 1]) for i in range(n_stage)] for j in range(5)]
+    step_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.warmup, args.warmup + args.steps)]
     dev_ms_total = sum(step_ms)
     dev_ms_total = max_over_ranks(dev_ms_total, pg, dev)
     ms_per_step = dev_ms_total / args.steps

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    griddep_launch_dependents();  // the next kernel may set up while this one runs
     const int hb = p.H * p.B;
     const int pair = p.n_pairs - 1 - (int)(blockIdx.x / hb);  // longest (causal) work first
     const int head = (int)(blockIdx.x % hb) % p.H;
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();  // Q/K/V and the cache were written by the previous kernels
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t sQ = smem_u32(smem + C::Q_OFF);
     const uint32_t sRing = smem_u32(smem + C::RING_OFF);
@@ -423,13 +425,13 @@ bool make_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4], cons
 template <int D>
 cudaError_t attn_launch(const AttnArgs& a, int* dev_err, cudaStream_t st) {
     using C = Cfg<D>;
-    static std::atomic<bool> attr[64];  // per device; racing first calls set the same attribute
+    static std::atomic<bool> smem_set[64];  // per device; racing first calls set the same attribute
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr[dev].load()) {
+    if (dev >= 0 && dev < 64 && !smem_set[dev].load()) {
         cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        attr[dev].store(true);
+        smem_set[dev].store(true);
     }
     const uint64_t rowlen = 3ull * a.hl * D;
     const uint64_t M = (uint64_t)a.B * a.Tq;
@@ -467,8 +469,19 @@ cudaError_t attn_launch(const AttnArgs& a, int* dev_err, cudaStream_t st) {
     p.timeout_ns = wait_timeout_ns();
     const long long grid = (long long)p.n_pairs * a.H * a.B;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    attn_tc_kernel<D><<<(unsigned)grid, AT_THREADS, C::SMEM, st>>>(mq, mk, mv, p);
-    return cudaGetLastError();
+    // programmatic dependent launch: CTAs may start while the previous kernel
+    // of the stream finishes (the kernel waits before its first read)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(AT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, mq, mk, mv, p);
 }
 
 }  // namespace

@@ -610,6 +610,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    griddep_launch_dependents();  // the next kernel may set up while this one runs
     // PAIR: rank in the cluster (0 issues the MMAs) and the item stream of the pair
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const int unit = PAIR ? (int)(blockIdx.x / 2) : (int)blockIdx.x;
@@ -640,6 +641,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // everything below may read what the previous kernel of the stream wrote
+    // (operands, residual, row scales) or reuse its scratch
+    griddep_wait();
     const int kbt = p.reduce ? p.shards * p.k_blocks : p.k_blocks;  // k-blocks per tile
 
     if (warp == 0) {
@@ -954,11 +958,13 @@ cudaError_t set_smem_attr() {
 // behind; the reductions at the end of the launch are left exposed
 // (SPLIT_COST_KB) and move every partial twice (written, read back):
 // about SPLIT_MB_PER_KB MB of that traffic over the whole GPU costs one
-// k-block of time (a k-block of a tile takes ~0.4 us; ~4 TB/s for the mixed
-// L2 / HBM traffic of the reductions).
+// k-block of time (a k-block of a tile takes ~0.4 us).  The two constants
+// were fitted to split / whole-tile timings of the 7B-shaped linears on a
+// B300 (M = 128 .. 4096): a split paid off only where it saved more than
+// ~10 us plus the traffic.
 constexpr int SPLIT_MAX_PARTS = 16, SPLIT_MIN_KB = 4, SPLIT_MAX_ROUNDS = SPLIT_ROUNDS_MAX, SPLIT_EPI_KB = 6,
-              SPLIT_COST_KB = 2;
-constexpr double SPLIT_MB_PER_KB = 1.6;
+              SPLIT_COST_KB = 24;
+constexpr double SPLIT_MB_PER_KB = 1.2;
 constexpr size_t FLAG_BYTES = 16384;  // [split tile][rank][epilogue warp][2] ints; split tiles < units <= SMs
 
 struct Decomp {
@@ -1045,24 +1051,23 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
         p.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + FLAG_BYTES);
     }
     const int units = d.units;
-    if constexpr (PAIR) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * units, 1, 1);
-        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM;
-        cfg.stream = st;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, tmA, tmW, p);
-    } else {
-        tc_gemm_kernel<false><<<units, NUM_THREADS, C::SMEM, st>>>(tmA, tmW, p);
-        return cudaGetLastError();
-    }
+    // programmatic dependent launch: this grid may start while the previous
+    // kernel of the stream finishes (the kernel waits before its first read)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((PAIR ? 2 : 1) * units, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR>, tmA, tmW, p);
 }
 
 }  // namespace

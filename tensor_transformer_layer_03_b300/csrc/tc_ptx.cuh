@@ -329,6 +329,17 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t base, uint32_t cols) 
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Let the next kernel of the stream (launched with programmatic stream
+// serialization) start its CTAs as this grid's CTAs leave SMs; it waits in
+// griddep_wait() before touching anything this grid writes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the previous kernel of the stream has completed and its memory
+// operations are visible (returns at once when there is none).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

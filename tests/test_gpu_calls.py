@@ -245,7 +245,7 @@ def test_attention_with_cache(tp, d, H, deg, B, T, pos, cap, dtype):
         assert np.array_equal(kn[b, :, pos + T:], np64(kc[b, :, pos + T:]), equal_nan=True)
 
 
-@pytest.mark.parametrize("deg,M", [(4, 2048), (2, 128), (4, 512)])
+@pytest.mark.parametrize("deg,M", [(4, 2048), (2, 128), (4, 512), (4, 4096)])
 def test_linears_split_tiles_7b(tp, deg, M):
     """The four linears of the 7B-shaped block at prompt sizes whose tiles
     do not fill the SMs evenly (the last round's tiles cut into parts,
@@ -289,11 +289,11 @@ def test_linears_split_tiles_7b(tp, deg, M):
         nw = float(np.max(np.abs(np64(out[rows]) - ref)) / np.max(np.abs(ref)))
         assert nw <= 1e-4, (name, M, deg, nw, sch.parts)
         assert_close_bf16(out_act[rows].cpu(), o.round_bf16(ref), f"{name} act copy M={M} tp{deg}")
-    # the headline prompt's QKV runs whole tiles and cut parts; the
-    # 128-token prompt (fewer tiles than SMs) cuts every O tile
-    if M == 2048:
-        s = plan.linear_schedule(0, tp.TP_QKV, M, nscr)
-        assert s.kernel == 0 and s.paired and s.parts > 1 and s.whole_tiles > 0
+    # the 128-token prompt (fewer tiles than SMs) cuts every O tile; the
+    # 4096-token prompt runs FFN-down's whole rounds and cuts its last one
     if M == 128:
         s = plan.linear_schedule(1, tp.TP_ATTN_OUT, M, nscr)
         assert s.kernel == 0 and not s.paired and s.parts > 1 and s.whole_tiles == 0
+    if M == 4096:
+        s = plan.linear_schedule(1, tp.TP_FFN_DOWN, M, nscr)
+        assert s.kernel == 0 and s.paired and s.parts > 1 and s.whole_tiles > 0
