@@ -482,14 +482,14 @@ def run_ours(args):
     stage_flops = [2.0 * M * d * 3 * d, attn, 2.0 * M * d * d, 2.0 * M * d * 2 * s.d_ffn, 2.0 * M * s.d_ffn * d]
     pk = peaks()
     achieved = stage_flops[dom] / (stage_mean[dom] / 1000.0) / 1e12
-    # DRAM traffic of the dominant kernel: null, because the GEMM kernel
-    # gained the pre-norm epilogue branches after its last ncu capture
-    # (profiles/tc_gemm_llama7b_prefill.md: 233.35 MB read + write per
-    # FFN-up launch before that change)
+    # DRAM traffic (read + write) per launch of each stage's kernel, from one
+    # ncu capture of this workload (profiles/tc_gemm_llama7b_prefill.md)
+    traffic = {"column_qkv": 150.24e6, "attention": 50.78e6, "row_o_reduce": 82.82e6,
+               "column_ffn_up_swiglu": 231.14e6, "row_ffn_down_reduce": 266.12e6}
     roofline = {"bound": "tensor", "kernel": stages[dom], "achieved": achieved, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
-                "traffic_last_capture": {"bytes": 233.35e6, "kernel_changed_since": True},
-                "peak_source": f"{pk['source']} bf16 dense burst (cuBLAS)"}
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic[stages[dom]],
+                "peak_source": f"{pk['source']} bf16 dense burst (cuBLAS)",
+                "timing": "per-stage CUDA events over a second timed pass of the same steps"}
 
     # end to end through the public call: every step copies its input X from
     # pinned host memory and reads its output Y back to pinned host memory.

@@ -59,15 +59,15 @@ __device__ __noinline__ inline bool mbar_wait_slow(uint64_t* bar, uint32_t parit
                                                    int* err, unsigned long long timeout_ns) {
     const uint32_t a = smem_u32(bar);
     const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > timeout_ns) {
-                *abort_flag = 1;
-                record_error(err, DEV_ERR_TIMEOUT);
-                return false;
-            }
+        // (each try_wait may suspend the thread for a while, so the abort
+        // flag and the clock are checked after every one)
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            record_error(err, DEV_ERR_TIMEOUT);
+            return false;
         }
     }
 }
@@ -89,25 +89,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __noinline__ inline bool mbar_wait_warp_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                         int* err, unsigned long long timeout_ns) {
     const uint32_t a = smem_u32(bar);
-    unsigned long long t0 = 0;
-    for (uint32_t it = 0;; ++it) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
         const bool ok = mbar_try_wait(a, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
-        if ((it & 31u) == 31u) {
-            int stop = 0;
-            if ((threadIdx.x & 31) == 0) {
-                const unsigned long long now = globaltimer();
-                if (t0 == 0) t0 = now;
-                if (*abort_flag) {
-                    stop = 1;
-                } else if (now - t0 > timeout_ns) {
-                    *abort_flag = 1;
-                    record_error(err, DEV_ERR_TIMEOUT);
-                    stop = 1;
-                }
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0) {
+            if (*abort_flag) {
+                stop = 1;
+            } else if (globaltimer() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                record_error(err, DEV_ERR_TIMEOUT);
+                stop = 1;
             }
-            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
         }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
 }
 
