@@ -25,6 +25,9 @@ Sources (cited by page title and section):
 * [BYTE] "Tensor Parallelism: Splitting One Layer Across GPUs" (byteledger),
   section "Interaction with the rest of serving": the KV cache is split along
   with the heads.
+* [SP] the same undercodenews page (?p=110319), section "What Undercode
+  Say": sequence parallelism spreads the sequence's tokens across the
+  devices, combined with tensor parallelism.
 * [DMAP] undercodenews "device-map-vs-tensor-parallelism-exposed", section
   "the Original": a model is a sequence of layers, each consuming the
   previous layer's output; device_map places whole layers on different
@@ -54,7 +57,15 @@ design notes):
   x / sqrt(mean(x^2) + eps) * g; RoPE rotates each head's dimension pairs
   (2i, 2i+1) of Q and K by the angle p * theta^(-2i/d_head) at absolute
   position p (the pairing of the original rotary-embedding formulation);
-  the KV cache holds the rotated keys.
+  the KV cache holds the rotated keys;
+* sequence parallelism (``sequence_parallel_block_forward``; [SP] names it
+  without its mechanics): the token rows of the flattened batch (row
+  b*T + t) are cut into tp contiguous slices of M/tp rows; outside the
+  tensor-parallel linears and attention, shard s holds only slice s (the
+  residual adds happen per slice); the all-reduce after a row-parallel
+  linear becomes a reduce-scatter (shard s receives the shard-order sum of
+  the partials' rows of its slice) and the input of a column-parallel
+  linear is the all-gather (concatenation in shard order) of the slices.
 
 Arrays may be numpy arrays or torch CPU tensors of any float dtype; every
 function returns float64 numpy arrays.
@@ -72,6 +83,7 @@ __all__ = [
     "multi_head_attention", "column_parallel_linear", "row_parallel_partials",
     "all_reduce_sum", "ffn", "block_forward", "sharded_block_forward",
     "stack_forward", "rms_norm", "rope", "fold_gains", "llama_block_forward",
+    "reduce_scatter_rows", "all_gather_rows", "sequence_parallel_block_forward",
 ]
 
 # ----------------------------------------------------------------------------
@@ -328,6 +340,75 @@ def sharded_block_forward(x, w: dict, n_heads: int, act: str, causal: bool, tp: 
         A_sh.append(a_b)
         U_sh.append(u_b)
     return Y, A_sh, U_sh
+
+
+def reduce_scatter_rows(partials, tp: int) -> list:
+    """[SP] reading: the reduce-scatter of the row-parallel partials ([M, n]
+    each, M divisible by tp): shard r receives, for the rows of its slice
+    [r*M/tp, (r+1)*M/tp) only, the sum of every shard's partial taken in
+    shard order."""
+    m = partials[0].shape[0]
+    ms = m // tp
+    out = []
+    for r in range(tp):
+        acc = np.zeros_like(to64(partials[0][r * ms:(r + 1) * ms]))
+        for p in partials:
+            acc = acc + to64(p[r * ms:(r + 1) * ms])
+        out.append(acc)
+    return out
+
+
+def all_gather_rows(slices) -> np.ndarray:
+    """[SP] reading: every shard's input rows, gathered from the shards'
+    slices in shard order."""
+    return np.concatenate([to64(s) for s in slices], axis=0)
+
+
+def sequence_parallel_block_forward(x, w: dict, n_heads: int, act: str, causal: bool, tp: int):
+    """The block with sequence parallelism around the tensor-parallel
+    regions ([SP] with [TPT] "the Original"): x [B, T, d], B*T divisible by
+    tp.  Shard s holds token rows slice s of x, H and Y; each column-parallel
+    linear reads the all-gathered rows, each row-parallel linear's partials
+    are reduce-scattered to the slices and the residual is added per slice.
+
+    Returns (Y [B, T, d] assembled from the slices, [Y slice per shard],
+    [H slice per shard])."""
+    x = to64(x)
+    B, T, d = x.shape
+    M = B * T
+    if M % tp:
+        raise ValueError("B*T must divide by tp")
+    ms = M // tp
+    dh = d // n_heads
+    h_l = n_heads // tp
+    Wq, Wk, Wv, Wo, Wd = (to64(w[n]) for n in ("Wq", "Wk", "Wv", "Wo", "Wd"))
+    up = {n: to64(w[n]) for n in ("Wg", "Wu", "W1") if n in w}
+    f_l = Wd.shape[1] // tp
+    x_sl = [x.reshape(M, d)[r * ms:(r + 1) * ms] for r in range(tp)]
+    # attention block: all-gather, column-parallel QKV and per-shard heads
+    xg = all_gather_rows(x_sl)
+    partials = []
+    for s in range(tp):
+        rows = slice(s * h_l * dh, (s + 1) * h_l * dh)
+        a_s = np.empty((M, h_l * dh))
+        for b in range(B):
+            xb = xg[b * T:(b + 1) * T]
+            a_s[b * T:(b + 1) * T] = multi_head_attention(linear(xb, Wq[rows]), linear(xb, Wk[rows]),
+                                                          linear(xb, Wv[rows]), h_l, causal)
+        partials.append(a_s @ Wo[:, rows].T)
+    h_sl = [x_sl[r] + rs for r, rs in enumerate(reduce_scatter_rows(partials, tp))]
+    # FFN block: all-gather, column-parallel up (+activation), row-parallel down
+    hg = all_gather_rows(h_sl)
+    partials = []
+    for s in range(tp):
+        cols = slice(s * f_l, (s + 1) * f_l)
+        if act == "swiglu":
+            u_s = silu(linear(hg, up["Wg"][cols])) * linear(hg, up["Wu"][cols])
+        else:
+            u_s = gelu_erf(linear(hg, up["W1"][cols]))
+        partials.append(u_s @ Wd[:, cols].T)
+    y_sl = [h_sl[r] + rs for r, rs in enumerate(reduce_scatter_rows(partials, tp))]
+    return all_gather_rows(y_sl).reshape(B, T, d), y_sl, h_sl
 
 
 def stack_forward(x, layers: list, n_heads: int, act: str, causal: bool, kcaches=None, vcaches=None,

@@ -513,6 +513,49 @@ def pin_llama_brute_force_bf16_storage(o):
     assert np.max(np.abs(Ya - Yb)) < 1e-12
 
 
+def pin_reduce_scatter_all_gather(o):
+    """The reduce-scatter followed by the all-gather is the all-reduce: the
+    slices' sums, gathered in shard order, equal the sum of the whole
+    partials, exactly (same terms, same order); each slice holds its own
+    rows; gathering returns what was sliced."""
+    rng = _rng(71)
+    for tp in (1, 2, 4, 8):
+        parts = [rng.standard_normal((16, 5)) for _ in range(tp)]
+        rs = o.reduce_scatter_rows(parts, tp)
+        assert len(rs) == tp and all(r.shape == (16 // tp, 5) for r in rs)
+        assert np.array_equal(o.all_gather_rows(rs), o.all_reduce_sum(parts))
+        # slice r of shard-order sums, written out with explicit loops
+        ms = 16 // tp
+        for r in range(tp):
+            for i in range(ms):
+                for c in range(5):
+                    acc = 0.0
+                    for p in parts:
+                        acc += p[r * ms + i, c]
+                    assert abs(rs[r][i, c] - acc) < 1e-12
+        x = rng.standard_normal((24, 3))
+        assert np.array_equal(o.all_gather_rows([x[i * 24 // tp:(i + 1) * 24 // tp] for i in range(tp)]), x)
+
+
+def pin_sequence_parallel_block(o):
+    """With the tokens sliced across the shards around the tensor-parallel
+    regions the block is unchanged: equal to the unsharded block for every
+    degree, batch 1 and 2, both activations, with and without the mask; the
+    slices are the output's contiguous row blocks."""
+    for act in ("swiglu", "gelu"):
+        for causal in (True, False):
+            rng = _rng(72 + (act == "gelu") + 2 * causal)
+            B, T, d, H, f = 2, 8, 16, 8, 24
+            w = _weights(rng, d, f, act)
+            x = rng.standard_normal((B, T, d))
+            Y, _, _ = o.block_forward(x, w, H, act, causal)
+            for tp in (1, 2, 4, 8):
+                Ys, ysl, hsl = o.sequence_parallel_block_forward(x, w, H, act, causal, tp)
+                assert np.max(np.abs(Ys - Y)) < 1e-11, (act, causal, tp)
+                assert len(ysl) == tp and ysl[0].shape == (B * T // tp, d)
+                assert np.max(np.abs(ysl[-1] - Y.reshape(B * T, d)[-(B * T // tp):])) < 1e-11
+
+
 def pin_round_fp32(o):
     """Round to fp32, nearest even: 1 + 2^-24 is a tie that goes down to 1,
     1 + 3 * 2^-24 goes up to 1 + 2^-22; against torch's float64 -> float32 cast."""

@@ -11,7 +11,8 @@ from pins import ALL_PINS
 real = {n: getattr(o, n) for n in ("attention_head", "linear", "silu", "gelu_erf", "all_reduce_sum",
                                    "block_forward", "round_bf16", "check_plan", "multi_head_attention",
                                    "softmax_rows", "row_parallel_partials", "column_parallel_linear",
-                                   "sharded_block_forward", "stack_forward", "rope", "rms_norm", "fold_gains")}
+                                   "sharded_block_forward", "stack_forward", "rope", "rms_norm", "fold_gains",
+                                   "reduce_scatter_rows", "all_gather_rows")}
 
 
 def _att_scale_dh(q, k, v, causal, q_pos0=0):
@@ -164,7 +165,26 @@ def _fold_attn_gain_on_ffn(w, storage):
     return real["fold_gains"](w, storage)
 
 
+def _rs_shifted(partials, tp):
+    # every shard receives its neighbour's slice
+    rs = real["reduce_scatter_rows"](partials, tp)
+    return rs[1:] + rs[:1]
+
+
+def _rs_own_partial_only(partials, tp):
+    # each shard keeps its own partial's rows instead of the sum
+    ms = partials[0].shape[0] // tp
+    return [o.to64(partials[r][r * ms:(r + 1) * ms]) for r in range(tp)]
+
+
+def _gather_reversed(slices):
+    return real["all_gather_rows"](list(slices)[::-1])
+
+
 MUTATIONS = {
+    "reduce-scatter hands out the wrong slice": ("reduce_scatter_rows", _rs_shifted),
+    "reduce-scatter skips the sum": ("reduce_scatter_rows", _rs_own_partial_only),
+    "all-gather in reverse shard order": ("all_gather_rows", _gather_reversed),
     "folded gain not rounded": ("fold_gains", _fold_unrounded),
     "weights rounded before folding": ("fold_gains", _fold_round_twice),
     "attention gain folded into the FFN": ("fold_gains", _fold_attn_gain_on_ffn),
