@@ -286,6 +286,53 @@ def bench_decode(args, dev, flush=None, batch=1, timeline=False, prenorm=False):
             **({"timeline": tl} if tl else {})}
 
 
+def bench_seq(args, dev, wl_name="llama7b_prefill", steps=50):
+    """The block with sequence parallelism (tp_block_forward_seq: x and Y as
+    tp slices of the token rows in padded regions) next to the plain block,
+    interleaved step by step on one box, L2 flushed between steps."""
+    import torch
+
+    from tensor_transformer_layer_03_b300 import inputs as I
+    from tensor_transformer_layer_03_b300.runtime import TPBlock
+    wl = I.WORKLOADS[wl_name]
+    gen = torch.Generator().manual_seed(0)
+    w = I.make_weights(wl.shape, wl.dtype, gen)
+    blk = TPBlock(wl.shape, wl.tp, wl.dtype, w, device=dev, max_batch=wl.batch, max_seq=wl.seq)
+    del w
+    B, T, d = wl.batch, wl.seq, wl.shape.d_model
+    M = B * T
+    x = torch.randn(B, T, d, generator=gen).to(torch.bfloat16).to(dev)
+    cap = M // wl.tp + 64
+    xs = torch.zeros(wl.tp, cap, d, dtype=torch.bfloat16, device=dev)
+    xs[:, :M // wl.tp] = x.reshape(wl.tp, M // wl.tp, d)
+    y = torch.empty(B, T, d, dtype=torch.float32, device=dev)
+    ys = torch.empty(wl.tp, cap, d, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    times = {"plain": [], "seq": []}
+    with torch.cuda.stream(st):
+        for i in range(3 + steps):
+            for kind in ("plain", "seq"):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                if kind == "plain":
+                    blk.forward(x, wl.causal, out=y, stream=st)
+                else:
+                    blk.forward_seq(xs, B, T, wl.causal, out_slices=ys, stream=st)
+                e1.record(st)
+                if i >= 3:
+                    times[kind].append((e0, e1))
+        st.synchronize()
+    blk.plan.sync_status(st)
+    med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in times.items()}
+    lin, attn = block_flops(wl)
+    return {"workload": wl.name + "_sequence_parallel", "tp_degree": wl.tp, "batch": B, "seq": T,
+            "slice_rows": M // wl.tp, "slice_region_rows": cap, "ms_per_block_seq": med["seq"],
+            "ms_per_block_plain": med["plain"], "tokens_per_s_seq": M / (med["seq"] / 1e3),
+            "tflops_seq": (lin + attn) / (med["seq"] / 1e3) / 1e12, "steps": steps}
+
+
 def run_sweep(args):
     """One JSON line per workload of the batch x prompt sweep (7B shape, tp 4)
     and of the tp sweep (13B shape, 4 x 1024 tokens): the whole block through
@@ -367,6 +414,8 @@ def run_sweep(args):
                       "tokens_per_s": wl.tokens / (ms / 1e3), "tflops": tf,
                       "frac_of_bf16_peak": tf / pk["bf16_tflops"]}), flush=True)
     del stk, x, y
+    torch.cuda.empty_cache()
+    print(json.dumps(bench_seq(args, dev)), flush=True)
     torch.cuda.empty_cache()
     # batched one-token decode at 1024 cached positions (7B shape, tp 2)
     for b in (1, 4, 16, 64):
@@ -596,6 +645,8 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=1)
     ap.add_argument("--timeline", action="store_true", help="with --decode-only: per-kernel device timeline")
     ap.add_argument("--prenorm", action="store_true", help="with --decode-only: the RMSNorm + RoPE block variant")
+    ap.add_argument("--seq", action="store_true",
+                    help="instead of the headline line: the sequence-parallel block next to the plain one")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the headline line: one line per batch/prompt and tp-sweep workload")
     args = ap.parse_args()
@@ -605,6 +656,10 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.seq:
+        import torch
+        print(json.dumps(bench_seq(args, torch.device("cuda", 0))), flush=True)
+        return 0
     if args.decode_only:
         import torch
         print(json.dumps(bench_decode(args, torch.device("cuda", 0), batch=args.decode_batch,

@@ -287,6 +287,47 @@ tp_status tp_stack_forward(tp_plan_t plan, int n_layers, const void* const* pack
                            void* stream);
 
 /*
+ * Sequence parallelism around the tensor-parallel regions (undercodenews.com/
+ * ?p=110319, "What Undercode Say": tensor parallelism is combined with
+ * sequence parallelism, which spreads the sequence's tokens across the
+ * devices; the mechanics below are the usual reading, not on the page).
+ * Outside the tensor-parallel linears and attention the M = batch*seq token
+ * rows (row b*seq + t) are held as tp slices: slice s = rows
+ * [s*M/tp, (s+1)*M/tp), stored from base + s * slice_stride elements of the
+ * buffer's own type, rows of d_model elements (so slices may live in
+ * separate, padded regions).  The all-reduce after a row-parallel linear
+ * becomes a reduce-scatter -- every row's shard-order sum (plus its
+ * residual) is written into its slice -- and a column-parallel linear reads
+ * the all-gather of the slices (its tensor-core GEMM reads the rows straight
+ * from the slices through its tensor map).  Results equal those of the
+ * plain calls on the concatenated rows.
+ * Requirements (else nothing is enqueued): bf16 plan (TP_ERR_UNSUPPORTED);
+ * M divisible by tp (TP_ERR_INVALID_DIM); M / tp and slice_stride multiples
+ * of 8 (TP_ERR_ALIGNMENT); slice_stride >= (M / tp) * d_model
+ * (TP_ERR_INVALID_DIM).  All three run on the tensor-core GEMMs.
+ *
+ * tp_column_linear_gather: as tp_column_linear, x given as slices
+ *   (device act); TP_ERR_UNSUPPORTED for a pre-norm plan, as there.
+ * tp_row_linear_reduce_scatter: as tp_row_linear_reduce, with residual
+ *   (nullable), out_f32 and out_act (nullable) given as slices, all with
+ *   slice_stride.
+ * tp_block_forward_seq: as tp_block_forward (same workspace, zero-filled
+ *   before first use; caches as there; pre-norm plans too: the norms run
+ *   on the slices' rows), x as slices x_stride apart, Y (fp32) written as
+ *   slices y_stride apart; H stays in the workspace.
+ */
+tp_status tp_column_linear_gather(tp_plan_t plan, int which, const void* x_slices, long long slice_stride, int M,
+                                  const void* packed, void* out_shards, void* scratch, size_t scratch_bytes,
+                                  void* stream);
+tp_status tp_row_linear_reduce_scatter(tp_plan_t plan, int which, const void* in_shards, int M, const void* packed,
+                                       const void* residual_slices, void* out_f32_slices, void* out_act_slices,
+                                       long long slice_stride, void* scratch, size_t scratch_bytes, void* stream);
+tp_status tp_block_forward_seq(tp_plan_t plan, const void* x_slices, long long x_stride, int batch, int seq,
+                               int causal, void* k_cache, void* v_cache, int cache_cap, int cache_pos,
+                               const void* packed, void* workspace, size_t ws_bytes, void* out_f32_slices,
+                               long long y_stride, void* stream);
+
+/*
  * Pre-norm (LLaMA-style) variant of the block.  Norms and rotary embedding
  * are not on the pages ("What Is Tensor Parallelism?", netray.co, and
  * undercodenews.com/?p=110319 shard only the linears and attention); this

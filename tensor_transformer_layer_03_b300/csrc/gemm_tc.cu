@@ -117,7 +117,52 @@ struct Params {
     const float* row_scale;
     int rope_cols, rope_dh, rope_seq;
     const float2* rope_cs;
+    // sequence-parallel layouts (see TcGemm): rows per slice (0: none), the
+    // row-parallel outputs' and residual's distance between slices, and the
+    // A rows staged per TMA box of a gathered column-parallel input
+    int slice_rows;
+    long long out_slice, res_slice;
+    int a_box;
 };
+
+// Element offset of row `row` (column 0) of a row-parallel output / of the
+// residual: plain [M][ldo], or slice row / slice_rows at `slice` elements
+// per slice.
+__device__ __forceinline__ long long out_row(const Params& p, int row) {
+    if (!p.slice_rows) return (long long)row * p.ldo;
+    return (long long)(row / p.slice_rows) * p.out_slice + (long long)(row % p.slice_rows) * p.ldo;
+}
+__device__ __forceinline__ long long res_row(const Params& p, int row) {
+    if (!p.slice_rows) return (long long)row * p.ldo;
+    return (long long)(row / p.slice_rows) * p.res_slice + (long long)(row % p.slice_rows) * p.ldo;
+}
+
+// Row offsets of an epilogue warp's 32-row block (rows row_base .. +31,
+// row_base a multiple of 32): when no slice boundary can fall inside the
+// block (plain layout, or slices of a multiple of 32 rows) the offsets are
+// the block's first row's plus r * ldo; otherwise each row is mapped.
+struct RowMap {
+    long long out0, res0;
+    int row_base;
+    bool fast;
+    __device__ __forceinline__ RowMap(const Params& p, int rb) {
+        row_base = rb;
+        fast = p.slice_rows == 0 || p.slice_rows % 32 == 0;
+        out0 = out_row(p, rb);
+        res0 = res_row(p, rb);
+    }
+    __device__ __forceinline__ long long out(const Params& p, int r) const {
+        return fast ? out0 + (long long)r * p.ldo : out_row(p, row_base + r);
+    }
+    __device__ __forceinline__ long long res(const Params& p, int r) const {
+        return fast ? res0 + (long long)r * p.ldo : res_row(p, row_base + r);
+    }
+};
+
+// Four consecutive finished row-parallel outputs at element offset o of
+// the output rows (residual already added): fp32 out + optional plan-dtype
+// copy.
+__device__ __forceinline__ void store_row4(const Params& p, long long o, float4 t);
 
 // Rotary position embedding of N consecutive values of one row starting at
 // column `col` of a shard (col a multiple of N, N a multiple of 4): pairs
@@ -251,17 +296,19 @@ __device__ __forceinline__ float4 load_res4(const Params& p, long long o) {
 }
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
+__device__ __forceinline__ void store_row4(const Params& p, long long o, float4 t) {
+    *reinterpret_cast<float4*>((float*)p.out + o) = t;
+    if (p.out2) *reinterpret_cast<uint2*>((bf16*)p.out2 + o) = pack_bf16x4(t);
+}
+
 // Four consecutive finished outputs (row, col .. col+3), residual already
 // added: row-parallel fp32 out + optional plan-dtype copy, or a
 // column-parallel bf16 store (activation already applied).
 __device__ __forceinline__ void store4(const Params& p, int shard, int row, int col, float4 t) {
-    if (p.epi == EPI_ROW_REDUCE) {
-        const long long o = (long long)row * p.ldo + col;
-        *reinterpret_cast<float4*>((float*)p.out + o) = t;
-        if (p.out2) *reinterpret_cast<uint2*>((bf16*)p.out2 + o) = pack_bf16x4(t);
-    } else {
+    if (p.epi == EPI_ROW_REDUCE)
+        store_row4(p, out_row(p, row) + col, t);
+    else
         *reinterpret_cast<uint2*>((bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo + col) = pack_bf16x4(t);
-    }
 }
 
 // Column-parallel per-element epilogue of N consecutive columns of one row
@@ -288,7 +335,7 @@ __device__ __forceinline__ void prefetch_residual(const Params& p, int lane, int
     if (r >= r1 || grow >= p.M) return;
     const int es = p.residual_f32 ? 4 : 2;
     const int ncols = min(HALF_N, p.N - col0);  // a multiple of 8
-    prefetch_l2((const char*)p.residual + ((long long)grow * p.ldo + col0) * es, (uint32_t)(ncols * es));
+    prefetch_l2((const char*)p.residual + (res_row(p, grow) + col0) * es, (uint32_t)(ncols * es));
 }
 
 // Whole tile of a column-parallel launch: this warp's 32 rows x 128
@@ -367,6 +414,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, fl
                                              int col0, float* rbuf) {
     constexpr int NC = HALF_N / 32;
     constexpr int L = 1;
+    const RowMap rm(p, row_base);
     if (RES != 0 && rbuf != nullptr) {
         // the unit's last tile: the ring is idle, so the whole residual
         // block (32 rows x 128 columns, 512-byte rows) is copied into this
@@ -378,7 +426,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, fl
 #pragma unroll 4
             for (int r = 0; r < 32; ++r) {
                 const int grow = row_base + r;
-                if (grow < p.M) cp_async16(sb + r * 512 + lane * 16, (const char*)p.residual + ((long long)grow * p.ldo + gcol) * ES);
+                if (grow < p.M) cp_async16(sb + r * 512 + lane * 16, (const char*)p.residual + (rm.res(p, r) + gcol) * ES);
             }
         }
         cp_async_wait_all();
@@ -400,7 +448,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, fl
                 if (RES == 2) t = add4(t, *reinterpret_cast<const float4*>(rbuf + rr * HALF_N + lc));
                 if (RES == 1) t = add4(t, bf16x4_to_float4(*reinterpret_cast<const uint2*>(
                                               reinterpret_cast<const char*>(rbuf) + rr * 512 + lc * 2)));
-                if (grow < p.M && gcol < p.N) store4(p, 0, grow, gcol, t);
+                if (grow < p.M && gcol < p.N) store_row4(p, rm.out(p, rr) + gcol, t);
             }
         }
         return;
@@ -409,7 +457,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, fl
     auto fetch = [=](int c0, int i) -> float4 {
         const int grow = row_base + 4 * i + (lane >> 3), gcol = c0 + 4 * (lane & 7);
         const bool ok = grow < p.M && gcol < p.N;
-        const long long o = (long long)grow * p.ldo + gcol;
+        const long long o = rm.res(p, 4 * i + (lane >> 3)) + gcol;
         if (RES == 1) {
             const uint2 r = ok ? *reinterpret_cast<const uint2*>((const bf16*)p.residual + o) : make_uint2(0u, 0u);
             return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), 0.f, 0.f);
@@ -440,7 +488,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, fl
                 t = add4(t, bf16x4_to_float4(make_uint2(__float_as_uint(rs[c % L][i].x), __float_as_uint(rs[c % L][i].y))));
             if (RES == 2) t = add4(t, rs[c % L][i]);
             if (RES != 0 && c + L < NC) rs[c % L][i] = fetch(cc + 32 * L, i);  // this slot's next use
-            if (grow < p.M && gcol < p.N) store4(p, 0, grow, gcol, t);
+            if (grow < p.M && gcol < p.N) store_row4(p, rm.out(p, 4 * i + (lane >> 3)) + gcol, t);
         }
     }
 }
@@ -489,6 +537,7 @@ __device__ __noinline__ bool wait_count(const int* cnt, int target, volatile int
 __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, long long pstride, int lane,
                                             int row_base, int r0, int r1, int shard, int col0, float* buf) {
     const int nr = r1 - r0;  // (parts + 1) * nr <= 48 rows of 512 bytes fit FIX_BYTES
+    const RowMap rm(p, row_base);
     const bool has_res = p.epi == EPI_ROW_REDUCE && p.residual != nullptr;
     const int es = p.residual_f32 ? 4 : 2;
     const uint32_t sb = smem_u32(buf);
@@ -503,7 +552,7 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, 
                 const int grow = row_base + r0 + j;
                 if (grow < p.M)
                     cp_async16(sb + res_off * 4 + j * 512 + lane * 16,
-                               (const char*)p.residual + ((long long)grow * p.ldo + gcol) * es);
+                               (const char*)p.residual + (rm.res(p, r0 + j) + gcol) * es);
             }
     }
     cp_async_wait_all();
@@ -545,7 +594,7 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, 
                 a = add4(a, es == 4 ? *reinterpret_cast<const float4*>(rrow + 16 * lane)
                                     : bf16x4_to_float4(*reinterpret_cast<const uint2*>(rrow + 8 * lane)));
             }
-            store4(p, shard, grow, gcol, a);
+            store_row4(p, rm.out(p, r0 + j) + gcol, a);
         } else {
             float v[4] = {a.x, a.y, a.z, a.w};
             col_epilogue<4>(p, grow, gcol, v);
@@ -671,11 +720,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // both CTAs' copies complete on the issuing CTA's barrier
                         const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
                         if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-                        tma_load_3d_pair(sa, &tmA, bar0, kk, a_row, p.reduce ? s : 0);
+                        if (p.a_box)
+                            for (int j = 0; j < A_ROWS; j += p.a_box)  // gathered rows: one box per slice piece
+                                tma_load_3d_pair(sa + j * BK * 2, &tmA, bar0, kk, (a_row + j) % p.slice_rows,
+                                                 (a_row + j) / p.slice_rows);
+                        else
+                            tma_load_3d_pair(sa, &tmA, bar0, kk, a_row, p.reduce ? s : 0);
                         tma_load_3d_pair(sa + C::A_BYTES, &tmW, bar0, kk, w_row, s);
                     } else {
                         mbar_expect_tx(&full[stage], C::STAGE_BYTES);
-                        tma_load_3d(sa, &tmA, smem_u32(&full[stage]), kk, a_row, p.reduce ? s : 0);
+                        if (p.a_box)
+                            for (int j = 0; j < A_ROWS; j += p.a_box)
+                                tma_load_3d(sa + j * BK * 2, &tmA, smem_u32(&full[stage]), kk, (a_row + j) % p.slice_rows,
+                                            (a_row + j) / p.slice_rows);
+                        else
+                            tma_load_3d(sa, &tmA, smem_u32(&full[stage]), kk, a_row, p.reduce ? s : 0);
                         tma_load_3d(sa + C::A_BYTES, &tmW, smem_u32(&full[stage]), kk, w_row, s);
                     }
                     if (++stage == C::STAGES) {
@@ -1010,9 +1069,22 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     using C = GCfg<PAIR>;
     CUtensorMap tmA, tmW;
     const uint64_t a_shards = g.reduce ? (uint64_t)g.shards : 1;
-    if (!make_map(&tmA, g.A, (uint64_t)g.K, (uint64_t)g.M, a_shards, (uint64_t)g.lda * 2,
-                  (uint64_t)g.M * g.lda * 2, A_ROWS))
+    int a_box = 0;
+    if (!g.reduce && g.slice_rows > 0) {
+        // gathered input [slices][slice_rows][K]: boxes of the largest power
+        // of two <= 128 rows dividing slice_rows, so that no box crosses a
+        // slice (slice_rows is a multiple of 8; each box lands on a 1 KB
+        // boundary of the stage, as the 128-byte swizzle needs)
+        a_box = A_ROWS;
+        while (g.slice_rows % a_box) a_box /= 2;
+        const uint64_t n_slices = (uint64_t)((g.M + g.slice_rows - 1) / g.slice_rows);
+        if (!make_map(&tmA, g.A, (uint64_t)g.K, (uint64_t)g.slice_rows, n_slices, (uint64_t)g.lda * 2,
+                      (uint64_t)g.a_slice * 2, (uint32_t)a_box))
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&tmA, g.A, (uint64_t)g.K, (uint64_t)g.M, a_shards, (uint64_t)g.lda * 2,
+                         (uint64_t)g.M * g.lda * 2, A_ROWS)) {
         return cudaErrorInvalidValue;
+    }
     if (!make_map(&tmW, g.W, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.shards, (uint64_t)g.K * 2,
                   (uint64_t)g.w_shard * 2, C::W_ROWS))
         return cudaErrorInvalidValue;
@@ -1041,6 +1113,10 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     p.rope_dh = g.rope_dh;
     p.rope_seq = g.rope_seq > 0 ? g.rope_seq : 1;
     p.rope_cs = g.rope_cs;
+    p.slice_rows = g.slice_rows > 0 ? g.slice_rows : 0;
+    p.out_slice = g.out_slice;
+    p.res_slice = g.res_slice;
+    p.a_box = a_box;
     const int kbt = (g.reduce ? g.shards : 1) * p.k_blocks;
     const Decomp d = choose_decomp(p.n_tiles, kbt, slots, C::RANKS, scratch ? scratch_bytes : 0);
     p.dp_items = d.dp;
@@ -1098,6 +1174,9 @@ TcSchedule tc_gemm_schedule(const TcGemm& g, size_t scratch_bytes, int sms, int 
 cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st) {
     if (g.epi == EPI_SWIGLU && (g.granule != 32 || g.N % 64 != 0)) return cudaErrorNotSupported;
     if (g.N % 8 != 0 || g.ldo % 8 != 0) return cudaErrorNotSupported;  // 4- and 8-wide vector stores
+    if (g.slice_rows < 0 || (g.slice_rows > 0 && (g.slice_rows % 8 != 0 || g.a_slice % 8 != 0 || g.out_slice % 8 != 0 ||
+                                                 g.res_slice % 8 != 0)))
+        return cudaErrorNotSupported;
     cudaError_t e = set_smem_attr<false>();
     if (e == cudaSuccess) e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;

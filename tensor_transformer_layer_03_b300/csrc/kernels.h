@@ -83,6 +83,13 @@ struct TcGemm {
     const float* row_scale;
     int rope_cols, rope_dh, rope_seq;
     const float2* rope_cs;
+    // sequence-parallel layouts (slice_rows > 0, a multiple of 8): row m of
+    // the token rows lives in slice m / slice_rows at row m % slice_rows;
+    // the slices of a column-parallel input A are a_slice elements apart,
+    // those of a row-parallel launch's out / out2 out_slice and of its
+    // residual res_slice apart (all multiples of 8)
+    int slice_rows;
+    long long a_slice, out_slice, res_slice;
 };
 bool tc_gemm_supported(int M, int N, int K);
 // scratch (nullable): the split tiles' counters (zero-filled before first
@@ -132,9 +139,10 @@ struct RopeTable {
 };
 // r[m] = 1 / sqrt(mean_c x[m][c]^2 + eps), x bf16 (x_f32 = 0) or fp32,
 // d a multiple of 8 and rows 16-byte aligned; the same launch fills
-// rope->cs when rope is non-null.
+// rope->cs when rope is non-null.  slice_rows > 0: row m of x lives in
+// slice m / slice_rows, slices slice_stride elements apart.
 cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, const RopeTable* rope,
-                     cudaStream_t st);
+                     cudaStream_t st, int slice_rows = 0, long long slice_stride = 0);
 
 // ---- tensor-core attention (attn_tc.cu) --------------------------------------
 bool tc_attention_supported(const AttnArgs& a);

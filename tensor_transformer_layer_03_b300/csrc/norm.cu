@@ -45,7 +45,7 @@ __device__ __forceinline__ float sumsq8(const float* p) {
 // parallelism).  Blocks past the first rms_blocks fill the rotary table.
 template <typename E>
 __global__ void rms_rows_k(const E* __restrict__ x, int M, int d, float eps, float* __restrict__ r, RopeTable rt,
-                           int rms_blocks) {
+                           int rms_blocks, int slice_rows, long long slice_stride) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if ((int)blockIdx.x >= rms_blocks) {
@@ -62,7 +62,9 @@ __global__ void rms_rows_k(const E* __restrict__ x, int M, int d, float eps, flo
     const int lane = threadIdx.x % 32;
     const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (row >= M) return;
-    const E* xr = x + (long long)row * d;
+    // (sequence-parallel input: row m in slice m / slice_rows)
+    const E* xr = x + (slice_rows ? (long long)(row / slice_rows) * slice_stride + (long long)(row % slice_rows) * d
+                                  : (long long)row * d);
     float s = 0.f;
     int c = lane * 8;
     for (; c + 3 * 256 < d; c += 4 * 256) {
@@ -90,7 +92,7 @@ cudaError_t scale_cols(int esize, void* W, long long rows, int d, const void* ga
 }
 
 cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r, const RopeTable* rope,
-                     cudaStream_t st) {
+                     cudaStream_t st, int slice_rows, long long slice_stride) {
     const int rms_blocks = (M + 7) / 8;
     RopeTable rt = {};
     if (rope) rt = *rope;
@@ -104,8 +106,11 @@ cudaError_t rms_rows(const void* x, int x_f32, int M, int d, float eps, float* r
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (x_f32) return cudaLaunchKernelEx(&cfg, rms_rows_k<float>, (const float*)x, M, d, eps, r, rt, rms_blocks);
-    return cudaLaunchKernelEx(&cfg, rms_rows_k<bf16>, (const bf16*)x, M, d, eps, r, rt, rms_blocks);
+    if (x_f32)
+        return cudaLaunchKernelEx(&cfg, rms_rows_k<float>, (const float*)x, M, d, eps, r, rt, rms_blocks, slice_rows,
+                                  slice_stride);
+    return cudaLaunchKernelEx(&cfg, rms_rows_k<bf16>, (const bf16*)x, M, d, eps, r, rt, rms_blocks, slice_rows,
+                              slice_stride);
 }
 
 }  // namespace tpk

@@ -118,9 +118,18 @@ tp_status attention_check(const tp_plan_s* p, int batch, int seq_q, const void* 
 
 // The block S1..S5 on a validated workspace layout; out_act (nullable)
 // receives a plan-dtype copy of Y (the next layer's input in a stack).
+// Sequence-parallel layout of the block's input x and output Y: token row
+// m in slice m / slice_rows, slices x_stride / y_stride elements apart
+// (slice_rows 0: the plain [M][d] layout).
+struct SeqLayout {
+    int slice_rows = 0;
+    long long x_stride = 0, y_stride = 0;
+};
+
 static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int seq, int causal, void* k_cache,
                                     void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
-                                    const Workspace& w, void* out_f32, void* out_act, void* stream);
+                                    const Workspace& w, void* out_f32, void* out_act, void* stream,
+                                    const SeqLayout& sp = SeqLayout());
 
 // Pre-norm extras of a column-parallel launch: row scales (1/rms of the
 // input rows) and the rotary embedding of the QKV output.
@@ -128,7 +137,14 @@ struct ColumnExtras {
     const float* row_scale = nullptr;
     const float2* rope_cs = nullptr;  // rotary (cos, sin) table, NULL: no rotation
     int rope_seq = 1;
+    int slice_rows = 0;               // sequence-parallel input: rows gathered from slices
+    long long a_slice = 0;            // elements between the input's slices
 };
+
+static tp_status row_linear_impl(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
+                                 const void* residual, void* out_f32, void* out_act, void* scratch,
+                                 size_t scratch_bytes, cudaStream_t st, int slice_rows = 0, long long res_slice = 0,
+                                 long long out_slice = 0);
 
 static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M, const void* packed,
                                     void* out_shards, void* scratch, size_t scratch_bytes, const ColumnExtras& ex,
@@ -169,6 +185,8 @@ static tpk::TcGemm column_gemm(const tp_plan_s* p, int which, const void* x, int
         g.rope_seq = ex.rope_seq;
         g.rope_cs = ex.rope_cs;
     }
+    g.slice_rows = ex.slice_rows;
+    g.a_slice = ex.a_slice;
     return g;
 }
 
@@ -224,8 +242,12 @@ tp_status tpk::status_from_cuda(cudaError_t e) {
 
 static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int seq, int causal, void* k_cache,
                                     void* v_cache, int cache_cap, int cache_pos, const void* packed, void* workspace,
-                                    const Workspace& w, void* out_f32, void* out_act, void* stream) {
+                                    const Workspace& w, void* out_f32, void* out_act, void* stream,
+                                    const SeqLayout& sp) {
     const int M = batch * seq;
+    // sequence-parallel: x and Y in slices; H stays in the workspace as
+    // contiguous slices (slice s = rows s * slice_rows.., the plain layout)
+    const long long h_slice = (long long)sp.slice_rows * p->d;
     void* qkv = ptr_at(workspace, w.qkv);
     void* attn = ptr_at(workspace, w.attn);
     void* hf32 = ptr_at(workspace, w.hf32);
@@ -249,13 +271,16 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
         rt.half = p->dh / 2;
         rt.log2_theta = p->rope_theta > 0.f ? log2f(p->rope_theta) : 0.f;
         const bool rope = p->rope_theta > 0.f;
-        cudaError_t e = tpk::rms_rows(x, p->dtype == TP_FP32, M, p->d, p->eps, r1, rope ? &rt : nullptr, st);
+        cudaError_t e = tpk::rms_rows(x, p->dtype == TP_FP32, M, p->d, p->eps, r1, rope ? &rt : nullptr, st,
+                                      sp.slice_rows, sp.x_stride);
         if (e != cudaSuccess) return cuda_status(e);
         ex1.row_scale = r1;
         ex1.rope_cs = rope ? rt.cs : nullptr;
         ex1.rope_seq = seq;
         ex2.row_scale = r2;
     }
+    ex1.slice_rows = sp.slice_rows;  // S1 gathers x from its slices
+    ex1.a_slice = sp.x_stride;
     tp_status s;
     {
         const Range r("S1 column QKV");
@@ -270,7 +295,8 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     if (s != TP_OK) return s;
     {
         const Range r("S3 row O + reduce");
-        s = tp_row_linear_reduce(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, stream);
+        s = row_linear_impl(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, st, sp.slice_rows, sp.x_stride,
+                            h_slice);
     }
     if (s != TP_OK) return s;
     if (p->llama) {  // RMSNorm of H: scale from the fp32 H, the GEMM reads its plan-dtype copy
@@ -284,7 +310,8 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     }
     if (s != TP_OK) return s;
     const Range r("S5 row FFN-down + reduce");
-    return tp_row_linear_reduce(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, out_act, gs, gsb, stream);
+    return row_linear_impl(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, out_act, gs, gsb, st, sp.slice_rows, h_slice,
+                           sp.y_stride);
 }
 
 extern "C" {
@@ -464,9 +491,13 @@ static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M
     const int epi = qkv ? tpk::EPI_STORE : (p->act == TP_ACT_SWIGLU ? tpk::EPI_SWIGLU : tpk::EPI_GELU);
     if (p->dtype == TP_BF16) {
         const tpk::TcGemm g = column_gemm(p, which, x, M, packed, out_shards, ex);
+        if (ex.slice_rows > 0)  // gathered rows: the tensor-core GEMM reads them through its tensor map
+            return tpk::tc_gemm_supported(M, g.N, g.K) ? run_linear(LK_TC, g, scratch, scratch_bytes, st)
+                                                       : TP_ERR_UNSUPPORTED;
         const LinearKernel k = pick_linear(p, g);
         if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st);
     }
+    if (ex.slice_rows > 0) return TP_ERR_UNSUPPORTED;
     if (ex.row_scale) return TP_ERR_UNSUPPORTED;  // (plan creation rules this out for pre-norm plans)
     tpk::SimtGemm g{};
     g.epi = epi;
@@ -500,16 +531,33 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
     if (misaligned(in_shards) || misaligned(packed) || misaligned(residual) || misaligned(out_f32) ||
         misaligned(out_act) || misaligned(scratch))
         return TP_ERR_ALIGNMENT;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return row_linear_impl(p, which, in_shards, M, packed, residual, out_f32, out_act, scratch, scratch_bytes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+static tp_status row_linear_impl(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
+                                 const void* residual, void* out_f32, void* out_act, void* scratch,
+                                 size_t scratch_bytes, cudaStream_t st, int slice_rows, long long res_slice,
+                                 long long out_slice) {
     const bool attn = which == TP_ATTN_OUT;
     const int ks = attn ? p->hl * p->dh : p->fl;
     const void* W = ptr_at(packed, attn ? p->off_o : p->off_down);
     const int res_f32 = attn ? (p->dtype == TP_FP32) : 1;
     if (p->dtype == TP_BF16) {
-        const tpk::TcGemm g = row_gemm(p, which, in_shards, M, packed, residual, out_f32, out_act);
+        tpk::TcGemm g = row_gemm(p, which, in_shards, M, packed, residual, out_f32, out_act);
+        if (slice_rows > 0) {  // reduce-scatter: the tensor-core GEMM writes each row into its slice
+            g.slice_rows = slice_rows;
+            g.res_slice = res_slice;
+            g.out_slice = out_slice;
+            return tpk::tc_gemm_supported(M, g.N, g.K) ? run_linear(LK_TC, g, scratch, scratch_bytes, st)
+                                                       : TP_ERR_UNSUPPORTED;
+        }
         const LinearKernel k = pick_linear(p, g);
         if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st);
     }
+    if (slice_rows > 0) return TP_ERR_UNSUPPORTED;
     tpk::SimtGemm g{};
     g.epi = tpk::EPI_ROW_REDUCE;
     g.is_bf16 = p->dtype == TP_BF16;
@@ -530,6 +578,78 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
     g.residual = residual;
     g.residual_f32 = res_f32;
     return cuda_status(tpk::simt_gemm(g, st));
+}
+
+// Checks of a sequence-parallel call: bf16 plan, M token rows in tp slices
+// of M / tp rows (a multiple of 8), slices `stride` elements apart (at
+// least a slice, a multiple of 8).
+static tp_status seq_check(const tp_plan_s* p, long long M, long long stride) {
+    if (p->dtype != TP_BF16) return TP_ERR_UNSUPPORTED;
+    if (M <= 0 || M % p->tp != 0) return TP_ERR_INVALID_DIM;
+    const long long ms = M / p->tp;
+    if (ms % 8 != 0 || stride % 8 != 0) return TP_ERR_ALIGNMENT;
+    if (stride < ms * p->d) return TP_ERR_INVALID_DIM;
+    return TP_OK;
+}
+
+extern "C" {
+
+tp_status tp_column_linear_gather(tp_plan_t p, int which, const void* x_slices, long long slice_stride, int M,
+                                  const void* packed, void* out_shards, void* scratch, size_t scratch_bytes,
+                                  void* stream) {
+    const Range trace_("tp_column_linear_gather");
+    if (!p || !x_slices || !packed || !out_shards) return TP_ERR_NULL_ARG;
+    if (M <= 0 || (which != TP_QKV && which != TP_FFN_UP)) return TP_ERR_INVALID_DIM;
+    if (misaligned(x_slices) || misaligned(packed) || misaligned(out_shards) || misaligned(scratch))
+        return TP_ERR_ALIGNMENT;
+    if (p->llama) return TP_ERR_UNSUPPORTED;
+    const tp_status c = seq_check(p, M, slice_stride);
+    if (c != TP_OK) return c;
+    ColumnExtras ex;
+    ex.slice_rows = M / p->tp;
+    ex.a_slice = slice_stride;
+    return column_linear_impl(p, which, x_slices, M, packed, out_shards, scratch, scratch_bytes, ex,
+                              static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_row_linear_reduce_scatter(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
+                                       const void* residual_slices, void* out_f32_slices, void* out_act_slices,
+                                       long long slice_stride, void* scratch, size_t scratch_bytes, void* stream) {
+    const Range trace_("tp_row_linear_reduce_scatter");
+    if (!p || !in_shards || !packed || !out_f32_slices) return TP_ERR_NULL_ARG;
+    if (M <= 0 || (which != TP_ATTN_OUT && which != TP_FFN_DOWN)) return TP_ERR_INVALID_DIM;
+    if (misaligned(in_shards) || misaligned(packed) || misaligned(residual_slices) || misaligned(out_f32_slices) ||
+        misaligned(out_act_slices) || misaligned(scratch))
+        return TP_ERR_ALIGNMENT;
+    const tp_status c = seq_check(p, M, slice_stride);
+    if (c != TP_OK) return c;
+    return row_linear_impl(p, which, in_shards, M, packed, residual_slices, out_f32_slices, out_act_slices, scratch,
+                           scratch_bytes, static_cast<cudaStream_t>(stream), M / p->tp, slice_stride, slice_stride);
+}
+
+tp_status tp_block_forward_seq(tp_plan_t p, const void* x_slices, long long x_stride, int batch, int seq,
+                               int causal, void* k_cache, void* v_cache, int cache_cap, int cache_pos,
+                               const void* packed, void* workspace, size_t ws_bytes, void* out_f32_slices,
+                               long long y_stride, void* stream) {
+    const Range trace_("tp_block_forward_seq");
+    if (!p || !x_slices || !packed || !workspace || !out_f32_slices) return TP_ERR_NULL_ARG;
+    if (batch <= 0 || seq <= 0) return TP_ERR_INVALID_DIM;
+    if (misaligned(workspace) || misaligned(x_slices) || misaligned(packed) || misaligned(out_f32_slices))
+        return TP_ERR_ALIGNMENT;
+    const long long M = (long long)batch * seq;
+    tp_status c = seq_check(p, M, x_stride);
+    if (c == TP_OK) c = seq_check(p, M, y_stride);
+    if (c != TP_OK) return c;
+    const tp_status chk = attention_check(p, batch, seq, k_cache, v_cache, cache_cap, cache_pos);
+    if (chk != TP_OK) return chk;
+    const Workspace w = workspace_layout(p, batch, seq);
+    if (ws_bytes < w.total) return TP_ERR_WORKSPACE_TOO_SMALL;
+    SeqLayout sp;
+    sp.slice_rows = (int)(M / p->tp);
+    sp.x_stride = x_stride;
+    sp.y_stride = y_stride;
+    return block_forward_impl(p, x_slices, batch, seq, causal, k_cache, v_cache, cache_cap, cache_pos, packed,
+                              workspace, w, out_f32_slices, nullptr, stream, sp);
 }
 
 tp_status tp_attention_heads(tp_plan_t p, const void* qkv_shards, int batch, int seq_q, int causal, void* k_cache,

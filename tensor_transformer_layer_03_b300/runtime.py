@@ -56,6 +56,22 @@ class TPBlock:
         return out
 
 
+    def forward_seq(self, x_slices: torch.Tensor, batch: int, seq: int, causal: bool, out_slices=None, k_cache=None,
+                    v_cache=None, cache_pos: int = 0, stream=None) -> torch.Tensor:
+        """Sequence-parallel layout: x_slices device [tp][cap][d] in the plan
+        dtype, slice s holding token rows s*M/tp .. (s+1)*M/tp - 1 of the
+        batch (M = batch * seq) in its first M/tp rows.  Returns Y fp32
+        [tp][cap][d] in the same layout (tp_block_forward_seq)."""
+        tp, cap, d = x_slices.shape
+        self.reserve(batch, seq)
+        if out_slices is None:
+            out_slices = torch.empty(tp, cap, d, dtype=torch.float32, device=self.device)
+        kcap = 0 if k_cache is None else k_cache.shape[2]
+        self.plan.block_forward_seq(x_slices, cap * d, batch, seq, causal, self.packed, self.workspace, out_slices,
+                                    out_slices.shape[1] * d, k_cache, v_cache, kcap, cache_pos, stream)
+        return out_slices
+
+
 class TPStack:
     """n_layers blocks of one shape, each with its own weights on ``device``,
     run through tp_stack_forward (the plan-dtype activation of layer l is the

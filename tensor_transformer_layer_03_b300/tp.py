@@ -58,6 +58,10 @@ EXPORTS = {
                               _i, _i, _p, _sz, _p, _p]),
     "tp_sync_status": (_i, [_p]),
     "tp_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+    "tp_column_linear_gather": (_i, [_p, _i, _p, ctypes.c_longlong, _i, _p, _p, _p, _sz, _p]),
+    "tp_row_linear_reduce_scatter": (_i, [_p, _i, _p, _i, _p, _p, _p, _p, ctypes.c_longlong, _p, _sz, _p]),
+    "tp_block_forward_seq": (_i, [_p, _p, ctypes.c_longlong, _i, _i, _i, _p, _p, _i, _i, _p, _p, _sz, _p,
+                                  ctypes.c_longlong, _p]),
     "tp_linear_schedule": (_i, [_p, _i, _i, _i, _sz, _i, _i, _p]),
 }
 
@@ -178,6 +182,27 @@ class Plan:
         nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
         check(tp_column_linear(self.handle, which, _ptr(x), M, _ptr(packed), _ptr(out), _ptr(scratch), nbytes,
                                _stream(stream)), "tp_column_linear")
+
+    def column_linear_gather(self, which, x_slices, slice_stride, M, packed, out, stream=None, scratch=None):
+        """x_slices: a tensor whose storage holds tp slices of M / tp rows,
+        slice_stride elements apart (tp_column_linear_gather)."""
+        nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+        check(tp_column_linear_gather(self.handle, which, _ptr(x_slices), slice_stride, M, _ptr(packed), _ptr(out),
+                                      _ptr(scratch), nbytes, _stream(stream)), "tp_column_linear_gather")
+
+    def row_linear_reduce_scatter(self, which, inp, M, packed, residual, out_f32, out_act, slice_stride, stream=None,
+                                  scratch=None):
+        nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+        check(tp_row_linear_reduce_scatter(self.handle, which, _ptr(inp), M, _ptr(packed), _ptr(residual),
+                                           _ptr(out_f32), _ptr(out_act), slice_stride, _ptr(scratch), nbytes,
+                                           _stream(stream)), "tp_row_linear_reduce_scatter")
+
+    def block_forward_seq(self, x_slices, x_stride, batch, seq, causal, packed, workspace, out_slices, y_stride,
+                          k_cache=None, v_cache=None, cache_cap=0, cache_pos=0, stream=None):
+        nbytes = workspace.numel() * workspace.element_size()
+        check(tp_block_forward_seq(self.handle, _ptr(x_slices), x_stride, batch, seq, 1 if causal else 0,
+                                   _ptr(k_cache), _ptr(v_cache), cache_cap, cache_pos, _ptr(packed), _ptr(workspace),
+                                   nbytes, _ptr(out_slices), y_stride, _stream(stream)), "tp_block_forward_seq")
 
     def row_linear_reduce(self, which, inp, M, packed, residual, out_f32, out_act=None, stream=None, scratch=None):
         nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()

@@ -243,3 +243,35 @@ def test_whole_block_calls_validate_before_the_first_launch(tp):
         assert B(h, good, 1, 4, 1, None, None, 0, 0, good, good, 1 << 30, odd, None) == 7    # out
         assert S(h, 2, arr, good, 1, 4, 1, arr, arr, 5, 2, good, 1 << 30, good, None) == 2   # cache bounds
         tp.tp_plan_destroy(h)
+
+
+def test_sequence_parallel_argument_validation(tp):
+    """The sequence-parallel calls check the slicing before anything is
+    enqueued: M divisible by tp, slices of a multiple of 8 rows, a stride of
+    at least one slice and a multiple of 8 elements, a bf16 plan."""
+    P = lambda v: ctypes.c_void_p(v)  # fake device addresses: never dereferenced
+    good, odd = P(0x10000), P(0x10008)
+    code, h = _create(tp, 256, 4, 1024, 2)  # bf16 SwiGLU, tp 2
+    assert code == 0
+    G, RS, BS = tp.tp_column_linear_gather, tp.tp_row_linear_reduce_scatter, tp.tp_block_forward_seq
+    d, ms = 256, 16                         # M = 32: two slices of 16 rows
+    assert G(None, 0, good, ms * d, 32, good, good, None, 0, None) == 1
+    assert G(h, 0, good, ms * d, 31, good, good, None, 0, None) == 2           # M not divisible by tp
+    assert G(h, 0, good, ms * d, 20, good, good, None, 0, None) == 7           # 10-row slices
+    assert G(h, 0, good, ms * d - 8, 32, good, good, None, 0, None) == 2       # stride below a slice
+    assert G(h, 0, good, ms * d + 4, 32, good, good, None, 0, None) == 7       # stride not a multiple of 8
+    assert G(h, 0, odd, ms * d, 32, good, good, None, 0, None) == 7
+    assert G(h, 2, good, ms * d, 32, good, good, None, 0, None) == 2
+    assert RS(h, 0, good, 32, good, None, None, None, ms * d, None, 0, None) == 1
+    assert RS(h, 1, good, 31, good, None, good, None, ms * d, None, 0, None) == 2
+    assert RS(h, 1, good, 32, good, odd, good, None, ms * d, None, 0, None) == 7
+    assert RS(h, 1, good, 32, good, None, good, None, 8, None, 0, None) == 2
+    assert BS(h, good, ms * d, 1, 32, 1, None, None, 0, 0, good, good, 64, good, ms * d, None) == 8  # workspace
+    assert BS(h, good, ms * d, 1, 31, 1, None, None, 0, 0, good, good, 1 << 30, good, ms * d, None) == 2
+    assert BS(h, good, ms * d, 1, 32, 1, None, None, 0, 0, good, good, 1 << 30, good, 8, None) == 2  # y stride
+    assert BS(h, None, ms * d, 1, 32, 1, None, None, 0, 0, good, good, 1 << 30, good, ms * d, None) == 1
+    tp.tp_plan_destroy(h)
+    code, h = _create(tp, 256, 4, 1024, 2, dtype=1)  # fp32 plan: no sequence-parallel kernels
+    assert code == 0
+    assert G(h, 0, good, ms * d, 32, good, good, None, 0, None) == 9
+    tp.tp_plan_destroy(h)
