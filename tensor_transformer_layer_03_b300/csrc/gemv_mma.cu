@@ -67,6 +67,10 @@ template <int NR>
 __device__ __forceinline__ void mma_dot(float (&d)[NR][4], const bf16* __restrict__ w0, const bf16* __restrict__ w1,
                                         long long ldw, const bf16* __restrict__ x, long long ldx, int M, int kb0,
                                         int kb1) {
+    // k-blocks per batch: the loads of batch j + 1 are issued before batch
+    // j's MMAs, so two batches are in flight per lane (software pipeline;
+    // the weight stream is latency-bound with only ~20 warps per SM)
+    constexpr int U = NR == 2 ? 2 : MU;
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const bool xv = g < M;
     const bf16* xr = x + (xv ? (long long)g * ldx : 0) + 8 * c;
@@ -74,25 +78,40 @@ __device__ __forceinline__ void mma_dot(float (&d)[NR][4], const bf16* __restric
     wl[0] = w0 + (long long)g * ldw + 8 * c;
     if (NR > 1) wl[NR - 1] = w1 + (long long)g * ldw + 8 * c;
     const long long hi_off = 8 * ldw;
-    int kb = kb0;
-    for (; kb + MU <= kb1; kb += MU) {
-        uint4 lo[NR][MU], hi[NR][MU], xx[MU];
+    struct Batch {
+        uint4 lo[NR][U], hi[NR][U], xx[U];
+    };
+    auto load = [&](Batch& b, int kb) {
 #pragma unroll
-        for (int u = 0; u < MU; ++u) {
+        for (int u = 0; u < U; ++u) {
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                lo[r][u] = ld_stream16(wl[r] + (kb + u) * 32);
-                hi[r][u] = ld_stream16(wl[r] + hi_off + (kb + u) * 32);
+                b.lo[r][u] = ld_stream16(wl[r] + (kb + u) * 32);
+                b.hi[r][u] = ld_stream16(wl[r] + hi_off + (kb + u) * 32);
             }
         }
 #pragma unroll
-        for (int u = 0; u < MU; ++u)
-            xx[u] = xv ? __ldg(reinterpret_cast<const uint4*>(xr + (kb + u) * 32)) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < U; ++u)
+            b.xx[u] = xv ? __ldg(reinterpret_cast<const uint4*>(xr + (kb + u) * 32)) : make_uint4(0, 0, 0, 0);
+    };
+    auto mma = [&](const Batch& b) {
 #pragma unroll
-        for (int u = 0; u < MU; ++u) {
+        for (int u = 0; u < U; ++u) {
 #pragma unroll
-            for (int r = 0; r < NR; ++r) kblock(d[r], lo[r][u], hi[r][u], xx[u]);
+            for (int r = 0; r < NR; ++r) kblock(d[r], b.lo[r][u], b.hi[r][u], b.xx[u]);
         }
+    };
+    int kb = kb0;
+    if (kb + U <= kb1) {
+        Batch cur, nxt;
+        load(cur, kb);
+        kb += U;
+        for (; kb + U <= kb1; kb += U) {
+            load(nxt, kb);
+            mma(cur);
+            cur = nxt;
+        }
+        mma(cur);
     }
     for (; kb < kb1; ++kb) {
         const uint4 xx = xv ? __ldg(reinterpret_cast<const uint4*>(xr + kb * 32)) : make_uint4(0, 0, 0, 0);
