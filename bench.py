@@ -52,36 +52,73 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms; only the
-    samples stamped inside the timed window [mark_start, mark_end] count."""
+    """SM clock, power and clock-event (throttle) reasons sampled during the
+    timed window [mark_start, mark_end]: read-only NVML queries from a
+    background thread every ~1 ms (so a window of a few ms still gets
+    samples), else nvidia-smi every 100 ms.  Nothing is ever set."""
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.out = ""
+    def __init__(self, gpu_index, period_s=0.001):
+        self.gpu, self.period = gpu_index, period_s
+        self.samples = []  # (time, sm_mhz, max_mhz, power_w, reasons)
         self.t0 = self.t1 = None
+        self.proc, self.out, self.thread, self.nvml = None, "", None, None
+        self._stop = False
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-        time.sleep(1.0)  # let nvidia-smi come up before the timed region
+            import ctypes
+            import threading
+            nv = ctypes.CDLL("libnvidia-ml.so.1")  # the driver's NVML, read-only queries below
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            clk_sm = ctypes.c_int(1)  # NVML_CLOCK_SM
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, clk_sm, ctypes.byref(mx))
+            # clock-event reason bits of nvml.h
+            bits = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nvml = nv
+
+            def loop():
+                sm, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop:
+                    if (nv.nvmlDeviceGetClockInfo(h, clk_sm, ctypes.byref(sm)) == 0 and
+                            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 and
+                            reasons_fn(h, ctypes.byref(rs)) == 0):
+                        self.samples.append((time.perf_counter(), sm.value, mx.value, pw.value / 1000.0,
+                                             [n for n, b in bits.items() if rs.value & b]))
+                    time.sleep(self.period)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+        except (OSError, AttributeError):
+            self.nvml = None
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                              "--format=csv,noheader,nounits", "-lms", "100"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+            time.sleep(1.0)  # let nvidia-smi come up before the timed region
         return self
 
     def mark_start(self):
-        self.t0 = datetime.datetime.now()
+        self.t0 = (time.perf_counter(), datetime.datetime.now())
 
     def mark_end(self):
-        self.t1 = datetime.datetime.now()
+        self.t1 = (time.perf_counter(), datetime.datetime.now())
 
     def stop(self):
+        self._stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
         if self.proc is not None:
             time.sleep(0.3)
             self.proc.terminate()
@@ -93,29 +130,34 @@ class ClockSampler:
 
     def summary(self):
         sm, mx, reasons, power = [], [], set(), []
-        for line in (self.out or "").splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 10:
-                continue
-            try:
-                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
-            except ValueError:
-                continue
-            if self.t0 is None or self.t1 is None or not (self.t0 <= ts <= self.t1):
-                continue
-            try:
-                sm.append(float(f[2]))
-                mx.append(float(f[3]))
-                power.append(float(f[4]))
-            except ValueError:
-                continue
-            for n, v in zip(self.NAMES, f[6:10]):
-                if v.lower() == "active":
-                    reasons.add(n)
+        if self.t0 is not None and self.t1 is not None:
+            for t, c, m, pw, rs in self.samples:
+                if self.t0[0] <= t <= self.t1[0]:
+                    sm.append(float(c))
+                    mx.append(float(m))
+                    power.append(pw)
+                    reasons.update(rs)
+            for line in (self.out or "").splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                    if not (self.t0[1] <= ts <= self.t1[1]):
+                        continue
+                    sm.append(float(f[2]))
+                    mx.append(float(f[3]))
+                    power.append(float(f[4]))
+                except ValueError:
+                    continue
+                for n, v in zip(self.NAMES, f[6:10]):
+                    if v.lower() == "active":
+                        reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_median": statistics.median(power)}
+                "samples": len(sm), "power_w_median": statistics.median(power),
+                "source": "nvml (read-only, ~1 ms)" if self.nvml else "nvidia-smi (100 ms)"}
 
 
 def dist_setup(ngpus):
@@ -172,6 +214,22 @@ def time_oracle(wl, sample_tokens, steps, warmup=0):
     return times
 
 
+def time_oracle_seq(wl, b):
+    """Seconds of one float64 oracle call on sequence b of the workload
+    (sequences are independent)."""
+    import torch
+
+    import oracle
+    from tensor_transformer_layer_03_b300 import inputs as I
+    gen = torch.Generator().manual_seed(0)
+    w = {k: oracle.to64(v) for k, v in I.make_weights(wl.shape, wl.dtype, gen).items()}
+    x = torch.randn(wl.batch, wl.seq, wl.shape.d_model, generator=gen).to(torch.bfloat16)
+    x = oracle.to64(x[b:b + 1])
+    t0 = time.perf_counter()
+    oracle.block_forward(x, w, wl.shape.n_heads, wl.shape.act, wl.causal)
+    return time.perf_counter() - t0
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -207,7 +265,7 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def bench_decode(args, dev, flush=None, batch=1, timeline=False, prenorm=False):
+def bench_decode(args, dev, flush=None, batch=1, timeline=False, prenorm=False, with_cpu=False):
     """One-token decode step of the 7B-shaped block (tp 2, 1024 cached
     positions + the new one) for `batch` sequences, captured in a CUDA graph;
     HBM GB/s against the algorithmic bytes (every packed weight once + the
@@ -278,12 +336,29 @@ def bench_decode(args, dev, flush=None, batch=1, timeline=False, prenorm=False):
     med = statistics.median(us)
     gbs = algo / (med * 1e-6) / 1e9
     pk = peaks()
+    cpu = None
+    if with_cpu:
+        # the float64 oracle on the same one-token step (batch B over the
+        # same cache), on the host cores
+        import oracle
+        inp = I.make_inputs(wl, seed=0)
+        w64 = {k: oracle.to64(v) for k, v in inp.items() if k.startswith("W")}
+        kc64, vc64 = oracle.to64(inp["Kcache"]), oracle.to64(inp["Vcache"])
+        x64 = oracle.to64(inp["X"])
+        t = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            oracle.block_forward(x64, w64, s.n_heads, s.act, True, kc64, vc64, P)
+            t.append(time.perf_counter() - t0)
+        sec = statistics.median(t)
+        cpu = {"value": B / sec, "unit": "tokens/s", "gb_s": algo / sec / 1e9, "cores": oracle_cores(), "kind": "oracle",
+               "sample": f"the whole step ({B} token(s) over {P} cached positions), float64 numpy oracle, median of 3"}
     return {"workload": "llama7b_decode" + ("_prenorm" if prenorm else ""), "tp_degree": wl.tp, "batch": B, "cache_positions": P + 1,
             "us_per_step_median": med, "us_per_step_p10": sorted(us)[len(us) // 10],
             "algorithmic_bytes": algo, "gb_s": gbs, "hbm_peak_gb_s": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
             "tokens_per_s": B / (med * 1e-6), "graph": True, "launches_per_step": n_launch,
             "l2": f"not flushed: each step streams {algo / 1e6:.1f} MB of weights and cache (> 126 MB L2)",
-            **({"timeline": tl} if tl else {})}
+            **({"timeline": tl} if tl else {}), **({"cpu_baseline": cpu} if cpu else {})}
 
 
 def bench_seq(args, dev, wl_name="llama7b_prefill", steps=50):
@@ -350,6 +425,7 @@ def run_sweep(args):
     wls.append(I.WORKLOADS["llama7b_prefill"].with_(name="llama7b_prefill_prenorm"))
     st = torch.cuda.Stream(device=dev)
     blk, key = None, None
+    cpu_done = set()
     for wl in wls:
         gen = torch.Generator().manual_seed(0)
         pre = wl.name.endswith("_prenorm")
@@ -382,9 +458,19 @@ def run_sweep(args):
         ms = statistics.median(a.elapsed_time(b) for a, b in evs)
         lin, attn = block_flops(wl)
         tf = (lin + attn) / (ms / 1e3) / 1e12
-        print(json.dumps({"workload": wl.name, "d_model": wl.shape.d_model, "tp_degree": wl.tp, "batch": wl.batch,
-                          "seq": wl.seq, "ms_per_block": ms, "tokens_per_s": wl.tokens / (ms / 1e3),
-                          "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "steps": n}), flush=True)
+        line = {"workload": wl.name, "d_model": wl.shape.d_model, "tp_degree": wl.tp, "batch": wl.batch,
+                "seq": wl.seq, "ms_per_block": ms, "tokens_per_s": wl.tokens / (ms / 1e3),
+                "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "steps": n}
+        if not args.no_cpu_baseline and not pre and (wl.shape, wl.batch, wl.seq) not in cpu_done:
+            # the float64 oracle (unsharded: the same for every degree) on the
+            # first and last sequences, per-sequence time x batch
+            cpu_done.add((wl.shape, wl.batch, wl.seq))
+            sec = statistics.mean(time_oracle_seq(wl, b) for b in sorted({0, wl.batch - 1}))
+            line["cpu_baseline"] = {"value": wl.seq / sec, "unit": "tokens/s", "cores": oracle_cores(),
+                                    "kind": "oracle", "sample": f"sequences {sorted({0, wl.batch - 1})} of {wl.batch}"
+                                    f" ({wl.seq} tokens each), float64 numpy oracle; tokens/s extrapolated to the"
+                                    f" batch as per-sequence time x {wl.batch}"}
+        print(json.dumps(line), flush=True)
         del x, y
     blk = None
     torch.cuda.empty_cache()
@@ -595,7 +681,8 @@ def run_ours(args):
                "ms_per_step": tot / args.steps, "pipelined": "copy-in / compute / copy-out streams, double buffers",
                "l2": "no flush; a step touches ~0.6 GB (> 126 MB L2)"}
 
-    decode = bench_decode(args, dev) if not args.no_decode else None
+    decode = (bench_decode(args, dev, with_cpu=(rank == 0 and world == 1 and not args.no_cpu_baseline))
+              if not args.no_decode else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
