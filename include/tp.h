@@ -148,10 +148,9 @@ tp_status tp_shard_weights(tp_plan_t plan, const void* Wq, const void* Wk, const
  *      TP_FFN_UP: n_s = d_ffn/tp, the activated U_s = silu(x Wg_s^T) *
  *                 (x Wu_s^T) (SwiGLU) or gelu(x W1_s^T) (GELU, erf form).
  *   scratch    device, nullable, scratch_bytes >= tp_linear_scratch_bytes(M)
- *              to be used; ZERO-FILLED before its first use (e.g. by
- *              cudaMemset), and every call that completes leaves its
- *              counters at zero again, so it can be reused without
- *              clearing (also across CUDA graph replays).  With it, a
+ *              to be used; contents on entry are ignored (a call that
+ *              splits tiles first clears the few KB of counters it uses,
+ *              on the same stream).  With it, a
  *              tensor-core GEMM whose output tiles would leave SMs idle in
  *              the last wave cuts each tile of that wave into equal
  *              k-parts on different SMs (run before the whole tiles): every
@@ -161,8 +160,7 @@ tp_status tp_shard_weights(tp_plan_t plan, const void* Wq, const void* Wk, const
  *              rows of the tile in part order 0, 1, ... and applies the
  *              epilogue -- inside the same launch, with no second pass.
  *              Calls in flight at the same time need separate
- *              scratch.  After tp_sync_status() reported
- *              TP_ERR_DEVICE_TIMEOUT, zero-fill the scratch again.
+ *              scratch.
  * M >= 1.
  */
 tp_status tp_column_linear(tp_plan_t plan, int which, const void* x, int M,
@@ -254,10 +252,9 @@ tp_status tp_attention_decode_noalloc(tp_plan_t plan, const void* qkv_shards, in
  *   x         device act [batch*seq][d_model]
  *   k_cache/v_cache/cache_cap/cache_pos   as in tp_attention_heads
  *   packed    device, from tp_shard_weights
- *   workspace device, ws_bytes >= tp_plan_sizes(batch, seq) workspace bytes,
- *             zero-filled before its first use (it holds the linears'
- *             scratch, see tp_column_linear); calls that complete leave it
- *             reusable without clearing
+ *   workspace device, ws_bytes >= tp_plan_sizes(batch, seq) workspace bytes
+ *             (contents on entry are ignored; it holds the linears'
+ *             scratch, see tp_column_linear)
  *   out_f32   device fp32 [batch*seq][d_model] = Y
  */
 tp_status tp_block_forward(tp_plan_t plan, const void* x, int batch, int seq, int causal,
@@ -277,8 +274,7 @@ tp_status tp_block_forward(tp_plan_t plan, const void* x, int batch, int seq, in
  *   packed_layers  host array of n_layers device pointers (tp_shard_weights)
  *   k_caches, v_caches  host arrays of n_layers device caches (as in
  *                  tp_attention_heads) or both NULL
- *   workspace      device, ws_bytes >= tp_stack_workspace_bytes(batch, seq),
- *                  zero-filled before its first use (as for tp_block_forward)
+ *   workspace      device, ws_bytes >= tp_stack_workspace_bytes(batch, seq)
  */
 tp_status tp_stack_workspace_bytes(tp_plan_t plan, int batch, int seq, size_t* bytes);
 tp_status tp_stack_forward(tp_plan_t plan, int n_layers, const void* const* packed_layers, const void* x,
@@ -311,8 +307,8 @@ tp_status tp_stack_forward(tp_plan_t plan, int n_layers, const void* const* pack
  * tp_row_linear_reduce_scatter: as tp_row_linear_reduce, with residual
  *   (nullable), out_f32 and out_act (nullable) given as slices, all with
  *   slice_stride.
- * tp_block_forward_seq: as tp_block_forward (same workspace, zero-filled
- *   before first use; caches as there; pre-norm plans too: the norms run
+ * tp_block_forward_seq: as tp_block_forward (same workspace; caches as
+ *   there; pre-norm plans too: the norms run
  *   on the slices' rows), x as slices x_stride apart, Y (fp32) written as
  *   slices y_stride apart; H stays in the workspace.
  */
@@ -363,8 +359,7 @@ tp_status tp_shard_weights_llama(tp_plan_t plan, const void* Wq, const void* Wk,
  * recorded by a bounded wait in this library's kernels on the current
  * device: TP_ERR_DEVICE_TIMEOUT, TP_ERR_CUDA on a CUDA error, else TP_OK.
  * After TP_ERR_DEVICE_TIMEOUT the outputs of the calls since the last
- * check are undefined and linear scratch / block workspaces they used must
- * be zero-filled again.  The device address of the error word (like that of
+ * check are undefined.  The device address of the error word (like that of
  * tp_attention_decode_noalloc's array) is looked up once per device and
  * kept for the life of the process: it does not survive cudaDeviceReset().
  */

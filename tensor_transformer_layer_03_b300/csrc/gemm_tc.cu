@@ -106,7 +106,7 @@ struct Params {
     // whole tiles' main loops follow them without a break.  Every part
     // writes its fp32 sums to `partials` ([item][rank][warp][32][128]) and
     // counts itself in (`flags`: [split tile][rank][warp] x {arrived,
-    // left}); at the end of the unit's work -- when this SM no longer
+    // left}, cleared by the host before the launch); at the end of the unit's work -- when this SM no longer
     // streams operands, so its loads are fast -- each part reduces its own
     // rows of the tile over all parts, in part order, and applies the
     // epilogue.
@@ -1125,6 +1125,11 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     if (d.parts > 1) {
         p.flags = static_cast<int*>(scratch);
         p.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + FLAG_BYTES);
+        // the split tiles' counters start at zero whatever the scratch held
+        // (a few KB; only launches that split pay for it)
+        const size_t flag_bytes = (size_t)(p.n_tiles - d.dp) * C::RANKS * EPI_WARPS * 2 * sizeof(int);
+        const cudaError_t e = cudaMemsetAsync(scratch, 0, flag_bytes, st);
+        if (e != cudaSuccess) return e;
     }
     const int units = d.units;
     // programmatic dependent launch: this grid may start while the previous

@@ -92,9 +92,9 @@ struct TcGemm {
     long long a_slice, out_slice, res_slice;
 };
 bool tc_gemm_supported(int M, int N, int K);
-// scratch (nullable): the split tiles' counters (zero-filled before first
-// use; every launch that completes leaves them zero) and fp32 partial sums;
-// at most tc_gemm_scratch_bytes() is touched.  Without scratch every launch
+// scratch (nullable): the split tiles' counters (cleared by the launch
+// itself) and fp32 partial sums; contents on entry do not matter; at most
+// tc_gemm_scratch_bytes() is touched.  Without scratch every launch
 // runs whole tiles only.
 size_t tc_gemm_scratch_bytes();
 cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st);

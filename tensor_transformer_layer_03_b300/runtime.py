@@ -12,10 +12,9 @@ from . import tp as _tp
 
 
 def _dev_bytes(nbytes: int, device) -> torch.Tensor:
-    # 16-byte aligned by the caching allocator (512-byte granularity); zero
-    # filled, as the block workspace and the linears' scratch must be before
-    # their first use
-    return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+    # 16-byte aligned by the caching allocator (512-byte granularity); the
+    # library ignores a workspace's contents on entry
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
 
 
 class TPBlock:

@@ -142,3 +142,26 @@ def test_llama7b_sweep_sampled(tp, B, T):
     seqs = sorted({0, B - 1})
     ex, st, _, _ = _oracle(("sweep", B, T), inp, wl, seqs=seqs)
     _check_block(y[seqs], ex, st, "bf16", f"7B sweep B{B} T{T} (sequences {seqs})")
+
+
+def test_workspace_reused_across_shapes():
+    """One workspace serves prompts of different sizes in turn: the linears'
+    split-tile counters sit at an offset that moves with the token count, on
+    bytes an earlier, larger call used for activations.  Every call must
+    still finish (no device timeout) and give the bits of a block whose
+    workspace holds an arbitrary byte pattern."""
+    shape, deg = I.LLAMA7B, 4
+    g = torch.Generator().manual_seed(21)
+    w = I.make_weights(shape, "bf16", g)
+    blk = TPBlock(shape, deg, "bf16", w, device=DEV)
+    fresh = TPBlock(shape, deg, "bf16", w, device=DEV)
+    for B, T in ((1, 2048), (4, 128), (1, 512), (2, 64), (1, 2048)):
+        x = torch.randn(B, T, shape.d_model, generator=g).to(torch.bfloat16).to(DEV)
+        y = blk.forward(x, True)
+        blk.plan.sync_status()
+        fresh.workspace = None
+        fresh.reserve(B, T)
+        fresh.workspace.fill_(0xA5)
+        y2 = fresh.forward(x, True)
+        fresh.plan.sync_status()
+        assert torch.equal(y, y2), (B, T)
