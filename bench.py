@@ -322,8 +322,9 @@ def bench_decode(args, dev, flush=None, batch=1, timeline=False, prenorm=False, 
                 for i in range(3):
                     graph.replay()
                 st.synchronize()
-            ks = sorted((e.time_range.start, e.time_range.end, e.name) for e in prof.events()
-                        if e.device_type.name == "CUDA")[-n_launch:]
+            allk = sorted((e.time_range.start, e.time_range.end, e.name) for e in prof.events()
+                          if e.device_type.name == "CUDA")
+            ks = allk[-(len(allk) // 3):]  # the last of the three replays (memsets included)
             t0 = ks[0][0]
             tl = [{"kernel": n.replace("(anonymous namespace)::", "").replace("void ", "").split("(")[0],
                    "start_us": round(a - t0, 2), "end_us": round(b - t0, 2)} for a, b, n in ks]

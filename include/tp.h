@@ -149,8 +149,9 @@ tp_status tp_shard_weights(tp_plan_t plan, const void* Wq, const void* Wk, const
  *                 (x Wu_s^T) (SwiGLU) or gelu(x W1_s^T) (GELU, erf form).
  *   scratch    device, nullable, scratch_bytes >= tp_linear_scratch_bytes(M)
  *              to be used; contents on entry are ignored (a call that
- *              splits tiles first clears the few KB of counters it uses,
- *              on the same stream).  With it, a
+ *              splits tiles first clears the 16 KB counter block at the
+ *              start of the scratch, on the same stream; the whole-block
+ *              calls clear it once for their four linears).  With it, a
  *              tensor-core GEMM whose output tiles would leave SMs idle in
  *              the last wave cuts each tile of that wave into equal
  *              k-parts on different SMs (run before the whole tiles): every

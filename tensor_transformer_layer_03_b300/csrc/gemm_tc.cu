@@ -106,7 +106,8 @@ struct Params {
     // whole tiles' main loops follow them without a break.  Every part
     // writes its fp32 sums to `partials` ([item][rank][warp][32][128]) and
     // counts itself in (`flags`: [split tile][rank][warp] x {arrived,
-    // left}, cleared by the host before the launch); at the end of the unit's work -- when this SM no longer
+    // left}: zero at the start of the launch, and the last part out of a
+    // block returns them to zero); at the end of the unit's work -- when this SM no longer
     // streams operands, so its loads are fast -- each part reduces its own
     // rows of the tile over all parts, in part order, and applies the
     // epilogue.
@@ -495,7 +496,8 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, fl
 
 // Part of a split tile: this warp's 32 rows x 128 columns of raw fp32 sums
 // to its partial block (row-major, 512-byte rows, coalesced).
-__device__ __forceinline__ void write_partial(uint32_t tbase, float* stg, int lane, float* part) {
+__device__ __forceinline__ void write_partial(uint32_t tbase, float* stg, int lane, float* part, int nrows) {
+    if (nrows <= 0) return;  // every row of this warp's block is past M
 #pragma unroll 1
     for (int c = 0; c < HALF_N / 32; ++c) {
         float v[32];
@@ -505,8 +507,9 @@ __device__ __forceinline__ void write_partial(uint32_t tbase, float* stg, int la
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            __stcg(reinterpret_cast<float4*>(part + (4 * i + (lane >> 3)) * HALF_N + 32 * c + 4 * (lane & 7)),
-                   stage_get(stg, lane, i));
+            if (4 * i + (lane >> 3) < nrows)  // rows past M are never read back
+                __stcg(reinterpret_cast<float4*>(part + (4 * i + (lane >> 3)) * HALF_N + 32 * c + 4 * (lane & 7)),
+                       stage_get(stg, lane, i));
     }
 }
 
@@ -605,9 +608,8 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, 
 
 // The reductions of a warp's pending split parts: items w0, w0 + n_units,
 // ... (n of them).  For each, wait (bounded) until all parts of its tile
-// have counted in, reduce this part's rows of the warp's block over all
-// parts, and count out; the last part out returns the tile's counters to
-// zero.  False when a wait gave up.
+// have counted in, reduce this part's rows of the warp's block (those
+// below M) over all parts, and count out.  False when a wait gave up.
 template <class C>
 __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_units, int kbt, uint32_t rank,
                                           int quarter, int half, int lane, volatile int* abort_flag, float* buf) {
@@ -622,17 +624,26 @@ __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_
         int m_blk, shard, n_blk;
         tile_coords(p, it.tile, C::GROUP_M, m_blk, shard, n_blk);
         const int row_base = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32;
+        if (row_base >= p.M) continue;  // the whole block is past M: its parts never counted in
         int* fl = p.flags + (((long long)(it.tile - p.dp_items) * C::RANKS + rank) * EPI_WARPS + qh) * 2;
-        int got = 1;
-        if (lane == 0) got = wait_count(fl, p.parts, abort_flag, p.err, p.timeout_ns) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) return false;
-        __threadfence();
-        const float* base0 = p.partials + ((long long)(it.sk - it.part) * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
-                             (long long)qh * PART_FLOATS;
-        reduce_rows(p, base0, pstride, lane, row_base, 32 * it.part / p.parts, 32 * (it.part + 1) / p.parts, shard,
-                    n_blk * BN + half * HALF_N, buf);
-        __syncwarp();
+        // this part's rows of the warp's 32, those past M dropped
+        const int r0 = 32 * it.part / p.parts;
+        const int r1 = min(32 * (it.part + 1) / p.parts, p.M - row_base);
+        if (r1 > r0) {
+            int got = 1;
+            if (lane == 0) got = wait_count(fl, p.parts, abort_flag, p.err, p.timeout_ns) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) return false;
+            __threadfence();
+            const float* base0 = p.partials +
+                                 ((long long)(it.sk - it.part) * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
+                                 (long long)qh * PART_FLOATS;
+            reduce_rows(p, base0, pstride, lane, row_base, r0, r1, shard, n_blk * BN + half * HALF_N, buf);
+            __syncwarp();
+        }
+        // count out; every part counted in before it counts out, so the
+        // last one out finds the block's parts all in and all done, and
+        // returns both counters to zero for the next launch on this scratch
         if (lane == 0) {
             if (atomicAdd(fl + 1, 1) == p.parts - 1) {
                 atomicExch(fl, 0);
@@ -875,7 +886,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
                 float* part = p.partials + ((long long)it.sk * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
                               (long long)qh * PART_FLOATS;
-                write_partial(tbase, stg, lane, part);
+                write_partial(tbase, stg, lane, part, p.M - row_base);
             }
             // the accumulator is in registers / memory now: hand TMEM back
             tc_fence_before();
@@ -891,7 +902,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int* fl = p.flags + (((long long)(it.tile - p.dp_items) * C::RANKS + rank) * EPI_WARPS + qh) * 2;
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atomicAdd(fl, 1);
+                if (lane == 0 && row_base < p.M) atomicAdd(fl, 1);
                 if (n_pend++ == 0) pend_w = it.sk;
             }
         }
@@ -1020,7 +1031,10 @@ cudaError_t set_smem_attr() {
 // k-block of time (a k-block of a tile takes ~0.4 us).  The two constants
 // were fitted to split / whole-tile timings of the 7B-shaped linears on a
 // B300 (M = 128 .. 4096): a split paid off only where it saved more than
-// ~10 us plus the traffic.
+// ~10 us plus the traffic.  Partial rows past M are neither written nor
+// read, so with fewer rows than a tile holds (few-token decode) the
+// traffic shrinks with the row fill, and so does the exposed reduction
+// (down to a quarter: its latency stays).
 constexpr int SPLIT_MAX_PARTS = 16, SPLIT_MIN_KB = 4, SPLIT_MAX_ROUNDS = SPLIT_ROUNDS_MAX, SPLIT_EPI_KB = 6,
               SPLIT_COST_KB = 24;
 constexpr double SPLIT_MB_PER_KB = 1.2;
@@ -1034,8 +1048,9 @@ struct Decomp {
 // Work decomposition over `units` co-resident units (SM pairs or SMs) for
 // T tiles of kbt k-blocks: the tiles that fill whole rounds run whole; the
 // remaining tiles are cut into equal k-parts (run first) so that the units
-// end evenly loaded.  The makespan (in k-blocks per unit) decides.
-Decomp choose_decomp(int T, int kbt, int units, int ranks, size_t scratch_bytes) {
+// end evenly loaded.  The makespan (in k-blocks per unit) decides.  fill:
+// the share of the tiles' rows that lie below M.
+Decomp choose_decomp(int T, int kbt, int units, int ranks, double fill, size_t scratch_bytes) {
     Decomp d{T, 1, T, T < units ? T : units, 0};
     long long best = (long long)((T + units - 1) / units) * kbt;
     if (scratch_bytes <= FLAG_BYTES) return d;
@@ -1048,9 +1063,10 @@ Decomp choose_decomp(int T, int kbt, int units, int ranks, size_t scratch_bytes)
         if (need > scratch_bytes) break;
         const long long rounds = (items + units - 1) / units;
         const long long per_item = (kbt + parts - 1) / parts;
-        const double traffic_mb = 2.0 * (double)items * ranks * A_ROWS * BN * sizeof(float) / 1e6;
+        const double traffic_mb = 2.0 * fill * (double)items * ranks * A_ROWS * BN * sizeof(float) / 1e6;
         const long long span = (long long)full * kbt + rounds * (per_item > SPLIT_EPI_KB ? per_item : SPLIT_EPI_KB) +
-                               SPLIT_COST_KB + (long long)(traffic_mb / SPLIT_MB_PER_KB);
+                               (long long)(SPLIT_COST_KB * (fill > 0.25 ? fill : 0.25)) +
+                               (long long)(traffic_mb / SPLIT_MB_PER_KB);
         if (span < best) {
             best = span;
             d.dp = full * units;
@@ -1065,7 +1081,7 @@ Decomp choose_decomp(int T, int kbt, int units, int ranks, size_t scratch_bytes)
 
 template <bool PAIR>
 cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch, size_t scratch_bytes,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool* counters_zero) {
     using C = GCfg<PAIR>;
     CUtensorMap tmA, tmW;
     const uint64_t a_shards = g.reduce ? (uint64_t)g.shards : 1;
@@ -1118,7 +1134,8 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     p.res_slice = g.res_slice;
     p.a_box = a_box;
     const int kbt = (g.reduce ? g.shards : 1) * p.k_blocks;
-    const Decomp d = choose_decomp(p.n_tiles, kbt, slots, C::RANKS, scratch ? scratch_bytes : 0);
+    const double fill = (double)g.M / ((double)p.m_blocks * C::TILE_M);
+    const Decomp d = choose_decomp(p.n_tiles, kbt, slots, C::RANKS, fill, scratch ? scratch_bytes : 0);
     p.dp_items = d.dp;
     p.parts = d.parts;
     p.n_items = d.n_items;
@@ -1126,10 +1143,13 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
         p.flags = static_cast<int*>(scratch);
         p.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + FLAG_BYTES);
         // the split tiles' counters start at zero whatever the scratch held
-        // (a few KB; only launches that split pay for it)
-        const size_t flag_bytes = (size_t)(p.n_tiles - d.dp) * C::RANKS * EPI_WARPS * 2 * sizeof(int);
-        const cudaError_t e = cudaMemsetAsync(scratch, 0, flag_bytes, st);
-        if (e != cudaSuccess) return e;
+        // (a few KB; only launches that split, and not already known to
+        // find them zero, pay for it)
+        if (!counters_zero || !*counters_zero) {
+            const cudaError_t e = cudaMemsetAsync(scratch, 0, FLAG_BYTES, st);
+            if (e != cudaSuccess) return e;
+        }
+        if (counters_zero) *counters_zero = true;
     }
     const int units = d.units;
     // programmatic dependent launch: this grid may start while the previous
@@ -1167,7 +1187,8 @@ TcSchedule tc_gemm_schedule(const TcGemm& g, size_t scratch_bytes, int sms, int 
     r.tiles = m_blocks * n_blocks * (g.reduce ? 1 : g.shards);
     r.kbt = (g.reduce ? g.shards : 1) * ((g.K + BK - 1) / BK);
     const int ranks = r.paired ? 2 : 1;
-    const Decomp d = choose_decomp(r.tiles, r.kbt, r.paired ? slots : sms, ranks, scratch_bytes);
+    const double fill = (double)g.M / ((double)m_blocks * tile_m);
+    const Decomp d = choose_decomp(r.tiles, r.kbt, r.paired ? slots : sms, ranks, fill, scratch_bytes);
     r.units = d.units;
     r.scratch_touched = d.scratch;
     r.whole = d.dp;
@@ -1176,7 +1197,8 @@ TcSchedule tc_gemm_schedule(const TcGemm& g, size_t scratch_bytes, int sms, int 
     return r;
 }
 
-cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st) {
+cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st,
+                    bool* counters_zero) {
     if (g.epi == EPI_SWIGLU && (g.granule != 32 || g.N % 64 != 0)) return cudaErrorNotSupported;
     if (g.N % 8 != 0 || g.ldo % 8 != 0) return cudaErrorNotSupported;  // 4- and 8-wide vector stores
     if (g.slice_rows < 0 || (g.slice_rows > 0 && (g.slice_rows % 8 != 0 || g.a_slice % 8 != 0 || g.out_slice % 8 != 0 ||
@@ -1188,9 +1210,9 @@ cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch
     // 2-SM tiles once there is more than one 128-row block of tokens
     if (g.M > A_ROWS) {
         const int slots = pair_slots();
-        if (slots > 0) return gemm_launch<true>(g, dev_err, slots, scratch, scratch_bytes, st);
+        if (slots > 0) return gemm_launch<true>(g, dev_err, slots, scratch, scratch_bytes, st, counters_zero);
     }
-    return gemm_launch<false>(g, dev_err, sm_count(), scratch, scratch_bytes, st);
+    return gemm_launch<false>(g, dev_err, sm_count(), scratch, scratch_bytes, st, counters_zero);
 }
 
 }  // namespace tpk

@@ -92,12 +92,15 @@ struct TcGemm {
     long long a_slice, out_slice, res_slice;
 };
 bool tc_gemm_supported(int M, int N, int K);
-// scratch (nullable): the split tiles' counters (cleared by the launch
-// itself) and fp32 partial sums; contents on entry do not matter; at most
-// tc_gemm_scratch_bytes() is touched.  Without scratch every launch
-// runs whole tiles only.
+// scratch (nullable): the split tiles' counters and fp32 partial sums; at
+// most tc_gemm_scratch_bytes() is touched.  Without scratch every launch
+// runs whole tiles only.  A launch that splits tiles clears the counters
+// first (a few KB, on `st`) unless *counters_zero says they are known to
+// be zero; it then sets *counters_zero, because a launch that completes
+// leaves them zero (a chain of launches on one scratch clears once).
 size_t tc_gemm_scratch_bytes();
-cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st);
+cudaError_t tc_gemm(const TcGemm& g, int* dev_err, void* scratch, size_t scratch_bytes, cudaStream_t st,
+                    bool* counters_zero = nullptr);
 // Host-only description of a tc_gemm launch on a GPU with `sms` SMs of which
 // `pair_slots` SM pairs can be co-resident (0: no paired launches).
 struct TcSchedule {

@@ -139,12 +139,13 @@ struct ColumnExtras {
     int rope_seq = 1;
     int slice_rows = 0;               // sequence-parallel input: rows gathered from slices
     long long a_slice = 0;            // elements between the input's slices
+    bool* counters_zero = nullptr;    // chain of launches on one scratch (see tpk::tc_gemm)
 };
 
 static tp_status row_linear_impl(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
                                  const void* residual, void* out_f32, void* out_act, void* scratch,
                                  size_t scratch_bytes, cudaStream_t st, int slice_rows = 0, long long res_slice = 0,
-                                 long long out_slice = 0);
+                                 long long out_slice = 0, bool* counters_zero = nullptr);
 
 static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M, const void* packed,
                                     void* out_shards, void* scratch, size_t scratch_bytes, const ColumnExtras& ex,
@@ -225,11 +226,13 @@ static LinearKernel pick_linear(const tp_plan_s* p, const tpk::TcGemm& g) {
 
 // Launch the bf16 linear `g` on the kernel pick_linear chose.
 static tp_status run_linear(LinearKernel k, const tpk::TcGemm& g, void* scratch, size_t scratch_bytes,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool* counters_zero = nullptr) {
     switch (k) {
         case LK_GEMV_MMA: return cuda_status(tpk::gemv_mma(g, st));
         case LK_GEMV: return cuda_status(tpk::gemv(g, device_error_word(), st));
-        case LK_TC: return cuda_status(tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st));
+        case LK_TC:
+            return cuda_status(
+                tpk::tc_gemm(g, device_error_word(), scratch, scratch ? scratch_bytes : 0, st, counters_zero));
         default: return TP_ERR_UNSUPPORTED;
     }
 }
@@ -258,7 +261,11 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float* r1 = reinterpret_cast<float*>(ptr_at(workspace, w.rs));
     float* r2 = r1 + M;
+    // the four linears share the split-tile scratch: the first that splits
+    // clears its counters, and each completed launch leaves them zero
+    bool cz = false;
     ColumnExtras ex1, ex2;
+    ex1.counters_zero = ex2.counters_zero = &cz;
     if (p->llama) {
         const Range r("RMSNorm(X) + rotary table");
         // RMSNorm of x (its gain is in the packed QKV rows) and, in the same
@@ -296,7 +303,7 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     {
         const Range r("S3 row O + reduce");
         s = row_linear_impl(p, TP_ATTN_OUT, attn, M, packed, x, hf32, hact, gs, gsb, st, sp.slice_rows, sp.x_stride,
-                            h_slice);
+                            h_slice, &cz);
     }
     if (s != TP_OK) return s;
     if (p->llama) {  // RMSNorm of H: scale from the fp32 H, the GEMM reads its plan-dtype copy
@@ -311,7 +318,7 @@ static tp_status block_forward_impl(tp_plan_t p, const void* x, int batch, int s
     if (s != TP_OK) return s;
     const Range r("S5 row FFN-down + reduce");
     return row_linear_impl(p, TP_FFN_DOWN, u, M, packed, hf32, out_f32, out_act, gs, gsb, st, sp.slice_rows, h_slice,
-                           sp.y_stride);
+                           sp.y_stride, &cz);
 }
 
 extern "C" {
@@ -492,10 +499,11 @@ static tp_status column_linear_impl(tp_plan_t p, int which, const void* x, int M
     if (p->dtype == TP_BF16) {
         const tpk::TcGemm g = column_gemm(p, which, x, M, packed, out_shards, ex);
         if (ex.slice_rows > 0)  // gathered rows: the tensor-core GEMM reads them through its tensor map
-            return tpk::tc_gemm_supported(M, g.N, g.K) ? run_linear(LK_TC, g, scratch, scratch_bytes, st)
-                                                       : TP_ERR_UNSUPPORTED;
+            return tpk::tc_gemm_supported(M, g.N, g.K)
+                       ? run_linear(LK_TC, g, scratch, scratch_bytes, st, ex.counters_zero)
+                       : TP_ERR_UNSUPPORTED;
         const LinearKernel k = pick_linear(p, g);
-        if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st);
+        if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st, ex.counters_zero);
     }
     if (ex.slice_rows > 0) return TP_ERR_UNSUPPORTED;
     if (ex.row_scale) return TP_ERR_UNSUPPORTED;  // (plan creation rules this out for pre-norm plans)
@@ -540,7 +548,7 @@ tp_status tp_row_linear_reduce(tp_plan_t p, int which, const void* in_shards, in
 static tp_status row_linear_impl(tp_plan_t p, int which, const void* in_shards, int M, const void* packed,
                                  const void* residual, void* out_f32, void* out_act, void* scratch,
                                  size_t scratch_bytes, cudaStream_t st, int slice_rows, long long res_slice,
-                                 long long out_slice) {
+                                 long long out_slice, bool* counters_zero) {
     const bool attn = which == TP_ATTN_OUT;
     const int ks = attn ? p->hl * p->dh : p->fl;
     const void* W = ptr_at(packed, attn ? p->off_o : p->off_down);
@@ -551,11 +559,12 @@ static tp_status row_linear_impl(tp_plan_t p, int which, const void* in_shards, 
             g.slice_rows = slice_rows;
             g.res_slice = res_slice;
             g.out_slice = out_slice;
-            return tpk::tc_gemm_supported(M, g.N, g.K) ? run_linear(LK_TC, g, scratch, scratch_bytes, st)
-                                                       : TP_ERR_UNSUPPORTED;
+            return tpk::tc_gemm_supported(M, g.N, g.K)
+                       ? run_linear(LK_TC, g, scratch, scratch_bytes, st, counters_zero)
+                       : TP_ERR_UNSUPPORTED;
         }
         const LinearKernel k = pick_linear(p, g);
-        if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st);
+        if (k != LK_SIMT) return run_linear(k, g, scratch, scratch_bytes, st, counters_zero);
     }
     if (slice_rows > 0) return TP_ERR_UNSUPPORTED;
     tpk::SimtGemm g{};
