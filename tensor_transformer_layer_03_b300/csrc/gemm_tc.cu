@@ -127,14 +127,16 @@ struct Params {
 };
 
 // Element offset of row `row` (column 0) of a row-parallel output / of the
-// residual: plain [M][ldo], or slice row / slice_rows at `slice` elements
-// per slice.
+// residual: plain [M][ldo] (SL false, the kernel instantiation for plain
+// layouts), or slice row / slice_rows at `slice` elements per slice.
+template <bool SL>
 __device__ __forceinline__ long long out_row(const Params& p, int row) {
-    if (!p.slice_rows) return (long long)row * p.ldo;
+    if (!SL) return (long long)row * p.ldo;
     return (long long)(row / p.slice_rows) * p.out_slice + (long long)(row % p.slice_rows) * p.ldo;
 }
+template <bool SL>
 __device__ __forceinline__ long long res_row(const Params& p, int row) {
-    if (!p.slice_rows) return (long long)row * p.ldo;
+    if (!SL) return (long long)row * p.ldo;
     return (long long)(row / p.slice_rows) * p.res_slice + (long long)(row % p.slice_rows) * p.ldo;
 }
 
@@ -142,22 +144,31 @@ __device__ __forceinline__ long long res_row(const Params& p, int row) {
 // row_base a multiple of 32): when no slice boundary can fall inside the
 // block (plain layout, or slices of a multiple of 32 rows) the offsets are
 // the block's first row's plus r * ldo; otherwise each row is mapped.
+template <bool SL>
 struct RowMap {
     long long out0, res0;
     int row_base;
     bool fast;
     __device__ __forceinline__ RowMap(const Params& p, int rb) {
         row_base = rb;
-        fast = p.slice_rows == 0 || p.slice_rows % 32 == 0;
-        out0 = out_row(p, rb);
-        res0 = res_row(p, rb);
+        fast = p.slice_rows % 32 == 0;
+        out0 = out_row<SL>(p, rb);
+        res0 = res_row<SL>(p, rb);
     }
     __device__ __forceinline__ long long out(const Params& p, int r) const {
-        return fast ? out0 + (long long)r * p.ldo : out_row(p, row_base + r);
+        return fast ? out0 + (long long)r * p.ldo : out_row<SL>(p, row_base + r);
     }
     __device__ __forceinline__ long long res(const Params& p, int r) const {
-        return fast ? res0 + (long long)r * p.ldo : res_row(p, row_base + r);
+        return fast ? res0 + (long long)r * p.ldo : res_row<SL>(p, row_base + r);
     }
+};
+// plain layout: row r of the block is row row_base + r of [M][ldo]
+template <>
+struct RowMap<false> {
+    int row_base;
+    __device__ __forceinline__ RowMap(const Params&, int rb) : row_base(rb) {}
+    __device__ __forceinline__ long long out(const Params& p, int r) const { return (long long)(row_base + r) * p.ldo; }
+    __device__ __forceinline__ long long res(const Params& p, int r) const { return (long long)(row_base + r) * p.ldo; }
 };
 
 // Four consecutive finished row-parallel outputs at element offset o of
@@ -302,14 +313,10 @@ __device__ __forceinline__ void store_row4(const Params& p, long long o, float4 
     if (p.out2) *reinterpret_cast<uint2*>((bf16*)p.out2 + o) = pack_bf16x4(t);
 }
 
-// Four consecutive finished outputs (row, col .. col+3), residual already
-// added: row-parallel fp32 out + optional plan-dtype copy, or a
-// column-parallel bf16 store (activation already applied).
+// Four consecutive finished column-parallel outputs (row, col .. col+3) of
+// a shard, activation already applied: a bf16 store.
 __device__ __forceinline__ void store4(const Params& p, int shard, int row, int col, float4 t) {
-    if (p.epi == EPI_ROW_REDUCE)
-        store_row4(p, out_row(p, row) + col, t);
-    else
-        *reinterpret_cast<uint2*>((bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo + col) = pack_bf16x4(t);
+    *reinterpret_cast<uint2*>((bf16*)p.out + shard * p.out_shard + (long long)row * p.ldo + col) = pack_bf16x4(t);
 }
 
 // Column-parallel per-element epilogue of N consecutive columns of one row
@@ -330,13 +337,14 @@ __device__ __forceinline__ void col_epilogue(const Params& p, int row, int col, 
 
 // The residual rows [r0, r1) of this warp's 32, columns col0 .. col0+127,
 // pulled into L2 ahead of the epilogue that adds them (one row per lane).
+template <bool SL>
 __device__ __forceinline__ void prefetch_residual(const Params& p, int lane, int row_base, int r0, int r1, int col0) {
     if (p.epi != EPI_ROW_REDUCE || p.residual == nullptr || col0 >= p.N) return;
     const int r = r0 + lane, grow = row_base + r;
     if (r >= r1 || grow >= p.M) return;
     const int es = p.residual_f32 ? 4 : 2;
     const int ncols = min(HALF_N, p.N - col0);  // a multiple of 8
-    prefetch_l2((const char*)p.residual + (res_row(p, grow) + col0) * es, (uint32_t)(ncols * es));
+    prefetch_l2((const char*)p.residual + (res_row<SL>(p, grow) + col0) * es, (uint32_t)(ncols * es));
 }
 
 // Whole tile of a column-parallel launch: this warp's 32 rows x 128
@@ -410,12 +418,12 @@ __device__ __forceinline__ float4 bf16x4_to_float4(uint2 r) {
 // about a microsecond while the tensor cores stream operands, so the
 // residual of chunk c + 1 is loaded while chunk c is stored (and the rows
 // were pulled into L2 while the MMAs ran).
-template <int RES>
+template <int RES, bool SL>
 __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, float* stg, int lane, int row_base,
                                              int col0, float* rbuf) {
     constexpr int NC = HALF_N / 32;
     constexpr int L = 1;
-    const RowMap rm(p, row_base);
+    const RowMap<SL> rm(p, row_base);
     if (RES != 0 && rbuf != nullptr) {
         // the unit's last tile: the ring is idle, so the whole residual
         // block (32 rows x 128 columns, 512-byte rows) is copied into this
@@ -537,10 +545,11 @@ __device__ __noinline__ bool wait_count(const int* cnt, int target, volatile int
 // between parts, `buf` this warp's share of the idle ring: every part's
 // rows and the residual rows are copied into it at once (one memory
 // latency for the whole reduction), then summed from shared memory.
+template <bool SL>
 __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, long long pstride, int lane,
                                             int row_base, int r0, int r1, int shard, int col0, float* buf) {
     const int nr = r1 - r0;  // (parts + 1) * nr <= 48 rows of 512 bytes fit FIX_BYTES
-    const RowMap rm(p, row_base);
+    const RowMap<SL> rm(p, row_base);
     const bool has_res = p.epi == EPI_ROW_REDUCE && p.residual != nullptr;
     const int es = p.residual_f32 ? 4 : 2;
     const uint32_t sb = smem_u32(buf);
@@ -610,7 +619,7 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, 
 // ... (n of them).  For each, wait (bounded) until all parts of its tile
 // have counted in, reduce this part's rows of the warp's block (those
 // below M) over all parts, and count out.  False when a wait gave up.
-template <class C>
+template <class C, bool SL>
 __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_units, int kbt, uint32_t rank,
                                           int quarter, int half, int lane, volatile int* abort_flag, float* buf) {
     const int qh = quarter * 2 + half;
@@ -638,7 +647,7 @@ __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_
             const float* base0 = p.partials +
                                  ((long long)(it.sk - it.part) * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
                                  (long long)qh * PART_FLOATS;
-            reduce_rows(p, base0, pstride, lane, row_base, r0, r1, shard, n_blk * BN + half * HALF_N, buf);
+            reduce_rows<SL>(p, base0, pstride, lane, row_base, r0, r1, shard, n_blk * BN + half * HALF_N, buf);
             __syncwarp();
         }
         // count out; every part counted in before it counts out, so the
@@ -654,7 +663,10 @@ __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_
     return true;
 }
 
-template <bool PAIR>
+// PAIR: 256-row tiles on an SM pair (cta_group::2), else 128-row tiles on
+// one SM.  SL: a sequence-parallel layout (gathered input rows or sliced
+// row-parallel outputs); the plain instantiation has none of its code.
+template <bool PAIR, bool SL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, Params p) {
     using C = GCfg<PAIR>;
@@ -731,7 +743,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // both CTAs' copies complete on the issuing CTA's barrier
                         const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
                         if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-                        if (p.a_box)
+                        if (SL && p.a_box)
                             for (int j = 0; j < A_ROWS; j += p.a_box)  // gathered rows: one box per slice piece
                                 tma_load_3d_pair(sa + j * BK * 2, &tmA, bar0, kk, (a_row + j) % p.slice_rows,
                                                  (a_row + j) / p.slice_rows);
@@ -740,7 +752,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_3d_pair(sa + C::A_BYTES, &tmW, bar0, kk, w_row, s);
                     } else {
                         mbar_expect_tx(&full[stage], C::STAGE_BYTES);
-                        if (p.a_box)
+                        if (SL && p.a_box)
                             for (int j = 0; j < A_ROWS; j += p.a_box)
                                 tma_load_3d(sa + j * BK * 2, &tmA, smem_u32(&full[stage]), kk, (a_row + j) % p.slice_rows,
                                             (a_row + j) / p.slice_rows);
@@ -838,7 +850,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int rb = m_blk * C::TILE_M + (int)rank * A_ROWS + quarter * 32;
             const int r0 = it.sk >= 0 ? 32 * it.part / p.parts : 0;
             const int r1 = it.sk >= 0 ? 32 * (it.part + 1) / p.parts : 32;
-            prefetch_residual(p, lane, rb, r0, r1, n_blk * BN + half * HALF_N);
+            prefetch_residual<SL>(p, lane, rb, r0, r1, n_blk * BN + half * HALF_N);
         };
         // A part's partial is written (and TMEM handed back) as soon as its
         // MMAs are done; its reduction waits for the end of the unit's work,
@@ -877,11 +889,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     Item nx;
                     float* rbuf = peek.next(p, nx) ? nullptr : fixbuf;  // last item: the ring is idle
                     if (p.residual == nullptr)
-                        epilogue_row<0>(p, tbase, stg, lane, row_base, col0, nullptr);
+                        epilogue_row<0, SL>(p, tbase, stg, lane, row_base, col0, nullptr);
                     else if (p.residual_f32)
-                        epilogue_row<2>(p, tbase, stg, lane, row_base, col0, rbuf);
+                        epilogue_row<2, SL>(p, tbase, stg, lane, row_base, col0, rbuf);
                     else
-                        epilogue_row<1>(p, tbase, stg, lane, row_base, col0, rbuf);
+                        epilogue_row<1, SL>(p, tbase, stg, lane, row_base, col0, rbuf);
                 }
             } else {
                 float* part = p.partials + ((long long)it.sk * C::RANKS + rank) * EPI_WARPS * PART_FLOATS +
@@ -907,7 +919,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         if (ok && n_pend > 0)
-            split_fixups<C>(p, pend_w, n_pend, n_units, kbt, rank, quarter, half, lane, abort_flag, fixbuf);
+            split_fixups<C, SL>(p, pend_w, n_pend, n_units, kbt, rank, quarter, half, lane, abort_flag, fixbuf);
     }
 
     tc_fence_before();
@@ -997,7 +1009,7 @@ int pair_slots() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true>, &cfg) != cudaSuccess || c <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true, false>, &cfg) != cudaSuccess || c <= 0) {
             cudaGetLastError();
             c = -1;
         }
@@ -1014,7 +1026,10 @@ cudaError_t set_smem_attr() {
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !done[dev].load()) {
         cudaError_t e =
-            cudaFuncSetAttribute(tc_gemm_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<PAIR>::SMEM);
+            cudaFuncSetAttribute(tc_gemm_kernel<PAIR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<PAIR>::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_gemm_kernel<PAIR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GCfg<PAIR>::SMEM);
         if (e != cudaSuccess) return e;
         done[dev].store(true);
     }
@@ -1168,7 +1183,12 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = PAIR ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR>, tmA, tmW, p);
+    // sliced layouts (a gathered input, or row-parallel outputs / residual in
+    // slices) take their own instantiation, so that the plain one carries
+    // neither the per-row slice mapping nor the gathered loads (in the
+    // producer's loop they cost the plain 7B prefill linears 5-12 us)
+    if (p.slice_rows > 0) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, true>, tmA, tmW, p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, false>, tmA, tmW, p);
 }
 
 }  // namespace
