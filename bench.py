@@ -620,8 +620,8 @@ def run_ours(args):
     achieved = stage_flops[dom] / (stage_mean[dom] / 1000.0) / 1e12
     # DRAM traffic (read + write) per launch of each stage's kernel, from one
     # ncu capture of this workload (profiles/tc_gemm_llama7b_prefill.md)
-    traffic = {"column_qkv": 150.24e6, "attention": 50.78e6, "row_o_reduce": 82.82e6,
-               "column_ffn_up_swiglu": 231.14e6, "row_ffn_down_reduce": 266.12e6}
+    traffic = {"column_qkv": 150.04e6, "attention": 50.92e6, "row_o_reduce": 84.70e6,
+               "column_ffn_up_swiglu": 230.69e6, "row_ffn_down_reduce": 266.54e6}
     roofline = {"bound": "tensor", "kernel": stages[dom], "achieved": achieved, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic[stages[dom]],
                 "peak_source": f"{pk['source']} bf16 dense burst (cuBLAS)",
