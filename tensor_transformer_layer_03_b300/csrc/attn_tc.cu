@@ -79,6 +79,33 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Three-input maximum and paired fp32 arithmetic (one instruction for two
+// lanes of work): the softmax thread issues about a third fewer
+// instructions per score.  Pairs are (first, second) = (low, high) word.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2split(unsigned long long r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // K-major operand: `bytes` into the tile along K (a multiple of 32 below 128
 // selects the 16-element K step inside the swizzle row; 64-column halves
 // follow each other HALF_BYTES apart).
@@ -304,13 +331,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     for (int i = 0; i < AT_KEYS; ++i)
                         if (i > lim) sv[i] = -INFINITY;
                 }
+                // row max over 8 independent chains, two new scores per step
                 float m8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+                for (int c = 0; c < 8; ++c) m8[c] = fmaxf(sv[2 * c], sv[2 * c + 1]);
 #pragma unroll
-                for (int i = 8; i < AT_KEYS; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
+                for (int k = 1; k < AT_KEYS / 16; ++k)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) m8[c] = max3f(m8[c], sv[16 * k + 2 * c], sv[16 * k + 2 * c + 1]);
+                const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], max3f(m8[5], m8[6], m8[7]))) *
                                  p.scale_log2;
                 // keep the stale max unless the row max grew by more than 2^8
                 const bool grow = j == 0 || mx > m_used + RESCALE_LOG2;
@@ -318,9 +347,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 const float corr = (j > 0 && grow) ? ex2(m_used - m_new) : 1.f;
                 m_used = m_new;
                 const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-                float rs8[8];
+                const unsigned long long scale2 = f2(p.scale_log2, p.scale_log2), negm2 = f2(neg_m, neg_m);
+                // row sum in 4 paired accumulators: pair k holds the partial
+                // sums of the columns 2i, 2i + 1 with i % 4 = k
+                unsigned long long rs2[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+                for (int k = 0; k < 4; ++k) rs2[k] = 0ull;
                 // P = 2^(s - m) as bf16 pairs written back over the first 64
                 // columns of this row of S (in registers already), where the
                 // P V product reads its A operand
@@ -329,14 +361,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float e0 = ex2(fmaf(sv[32 * q + 2 * i], p.scale_log2, neg_m));
-                        const float e1 = ex2(fmaf(sv[32 * q + 2 * i + 1], p.scale_log2, neg_m));
-                        rs8[(2 * i) & 7] += e0;
-                        rs8[(2 * i + 1) & 7] += e1;
+                        float a0, a1;
+                        f2split(fma2(f2(sv[32 * q + 2 * i], sv[32 * q + 2 * i + 1]), scale2, negm2), a0, a1);
+                        const float e0 = ex2(a0), e1 = ex2(a1);
+                        rs2[i & 3] = add2(rs2[i & 3], f2(e0, e1));
                         pk[i] = pack_bf16x2(e0, e1);
                     }
                     tmem_st16u(tS + 16 * q, pk);
                 }
+                float rs8[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) f2split(rs2[k], rs8[2 * k], rs8[2 * k + 1]);
                 const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 // the scores are dead here: rescale this row of O (rare) before
                 // the next P V accumulates into it
