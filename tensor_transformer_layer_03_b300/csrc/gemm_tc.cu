@@ -298,14 +298,6 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 
 __device__ __forceinline__ uint2 pack_bf16x4(float4 t) { return make_uint2(pack_bf16x2(t.x, t.y), pack_bf16x2(t.z, t.w)); }
 
-// Four consecutive residual values (row, col .. col+3), as fp32.
-__device__ __forceinline__ float4 load_res4(const Params& p, long long o) {
-    if (p.residual_f32) return *reinterpret_cast<const float4*>((const float*)p.residual + o);
-    const uint2 r = *reinterpret_cast<const uint2*>((const bf16*)p.residual + o);
-    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
-    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
-    return make_float4(r0.x, r0.y, r1.x, r1.y);
-}
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
 __device__ __forceinline__ void store_row4(const Params& p, long long o, float4 t) {

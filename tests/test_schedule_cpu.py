@@ -148,3 +148,18 @@ def test_schedule_query_argument_checks(tp):
     assert tp.tp_linear_schedule(plan.handle, 0, 0, 0, 0, SMS, PAIRS, ptr) == 2
     assert tp.tp_linear_schedule(plan.handle, 2, 0, 64, 0, SMS, PAIRS, ptr) == 2
     assert tp.tp_linear_schedule(plan.handle, 0, 0, 64, 0, 0, PAIRS, ptr) == 2
+
+
+def test_schedule_few_rows(tp):
+    """Batched decode above 8 rows (7B block, tp 2): a 16-row tile holds 1/8
+    of a full tile's rows, so its partials are 1/8 as large and cutting the
+    48 QKV tiles into parts that fill the SMs pays; at 128 rows (a full
+    tile) the same 48 tiles stay whole."""
+    plan = tp.Plan(4096, 32, 11008, 2)
+    n16 = plan.linear_scratch_bytes(16)
+    s = plan.linear_schedule(0, tp.TP_QKV, 16, n16, SMS, PAIRS)
+    assert (s.kernel, s.paired, s.tiles) == (0, 0, 48) and s.parts >= 2 and s.items <= SMS
+    assert s.whole_tiles == 0 and s.items == 48 * s.parts
+    n128 = plan.linear_scratch_bytes(128)
+    s = plan.linear_schedule(0, tp.TP_QKV, 128, n128, SMS, PAIRS)
+    assert (s.tiles, s.parts, s.whole_tiles) == (48, 1, 48)
