@@ -383,7 +383,7 @@ void tp_set_wait_timeout_ns(unsigned long long ns);
  * TP_ATTN_OUT / TP_FFN_DOWN, row = 1) would run M token rows with a linear
  * scratch of scratch_bytes, on a GPU with `sms` SMs of which `pair_slots`
  * SM pairs fit at once (148 and 74 on a B300).  kernel: 0 tensor-core
- * GEMM, 1 weight streaming on the tensor cores (2..8 rows), 2 weight
+ * GEMM, 1 weight streaming on the tensor cores (2..32 rows), 2 weight
  * streaming on the CUDA cores, 3 fp32 CUDA-core GEMM.  For kernel 0: tiles
  * (256 x 256 on SM pairs when paired, else 128 x 256), k-blocks of 64 per
  * tile, the tiles run whole, the parts each remaining tile is cut into

@@ -1,4 +1,4 @@
-// Weight streaming for 2..8 token rows with the products on the tensor
+// Weight streaming for 2..32 token rows with the products on the tensor
 // cores (the batched one-token decode step).
 //
 // At a handful of rows the linears still read every weight byte once and
@@ -13,7 +13,10 @@
 // memory element sits in which k slot; lane (g, c) loads elements
 // [8c, 8c + 8) of weight rows g and g + 8 and of token row g, and the first
 // four of them fill its slots {2c, 2c+1, 2c+8, 2c+9} of one MMA, the last
-// four those of the second.
+// four those of the second.  Above 8 token rows the same weight registers
+// meet NT = 2 or 4 groups of 8 token rows (lane (g, c) also loads token
+// rows g + 8, g + 16, ...): the weight stream, which is what costs, is read
+// once whatever the row count.
 //
 // Layout of the work (as in the other linears: undercodenews.com/?p=110319,
 // "the Original"): a block owns 16 output rows of one shard (column-
@@ -59,27 +62,33 @@ __device__ __forceinline__ void kblock(float (&d)[4], const uint4& lo, const uin
     mma_bf16_16816(d, lo.z, hi.z, lo.w, hi.w, x.z, x.w);
 }
 
-// d[r] += rows [0, 16) of group r (w0: group 0, w1: group 1; row stride ldw)
-// times token rows [0, M) of x (stride ldx; rows >= M count as zero) over
-// the k-blocks [kb0, kb1).  Accumulator element j of lane (g, c): row
-// g + 8 * (j / 2), token 2c + j % 2.
-template <int NR>
-__device__ __forceinline__ void mma_dot(float (&d)[NR][4], const bf16* __restrict__ w0, const bf16* __restrict__ w1,
-                                        long long ldw, const bf16* __restrict__ x, long long ldx, int M, int kb0,
-                                        int kb1) {
+// d[r][t] += rows [0, 16) of group r (w0: group 0, w1: group 1; row stride
+// ldw) times token rows [8t, 8t + 8) of x (stride ldx; rows >= M count as
+// zero) over the k-blocks [kb0, kb1).  Accumulator element j of lane
+// (g, c) in d[r][t]: row g + 8 * (j / 2), token 8t + 2c + j % 2.
+template <int NR, int NT>
+__device__ __forceinline__ void mma_dot(float (&d)[NR][NT][4], const bf16* __restrict__ w0,
+                                        const bf16* __restrict__ w1, long long ldw, const bf16* __restrict__ x,
+                                        long long ldx, int M, int kb0, int kb1) {
     // k-blocks per batch: the loads of batch j + 1 are issued before batch
     // j's MMAs, so two batches are in flight per lane (software pipeline;
-    // the weight stream is latency-bound with only ~20 warps per SM)
-    constexpr int U = NR == 2 ? 2 : MU;
+    // the weight stream is latency-bound with only ~20 warps per SM); fewer
+    // per batch with more token groups (registers)
+    constexpr int U = NT == 1 ? (NR == 2 ? 2 : MU) : (NT == 2 ? 2 : 1);
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    const bool xv = g < M;
-    const bf16* xr = x + (xv ? (long long)g * ldx : 0) + 8 * c;
+    bool xv[NT];
+    const bf16* xr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        xv[t] = g + 8 * t < M;
+        xr[t] = x + (xv[t] ? (long long)(g + 8 * t) * ldx : 0) + 8 * c;
+    }
     const bf16* wl[NR];
     wl[0] = w0 + (long long)g * ldw + 8 * c;
     if (NR > 1) wl[NR - 1] = w1 + (long long)g * ldw + 8 * c;
     const long long hi_off = 8 * ldw;
     struct Batch {
-        uint4 lo[NR][U], hi[NR][U], xx[U];
+        uint4 lo[NR][U], hi[NR][U], xx[NT][U];
     };
     auto load = [&](Batch& b, int kb) {
 #pragma unroll
@@ -91,14 +100,18 @@ __device__ __forceinline__ void mma_dot(float (&d)[NR][4], const bf16* __restric
             }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            b.xx[u] = xv ? __ldg(reinterpret_cast<const uint4*>(xr + (kb + u) * 32)) : make_uint4(0, 0, 0, 0);
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                b.xx[t][u] = xv[t] ? __ldg(reinterpret_cast<const uint4*>(xr[t] + (kb + u) * 32)) : make_uint4(0, 0, 0, 0);
     };
     auto mma = [&](const Batch& b) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
 #pragma unroll
-            for (int r = 0; r < NR; ++r) kblock(d[r], b.lo[r][u], b.hi[r][u], b.xx[u]);
+            for (int r = 0; r < NR; ++r)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) kblock(d[r][t], b.lo[r][u], b.hi[r][u], b.xx[t][u]);
         }
     };
     int kb = kb0;
@@ -114,34 +127,44 @@ __device__ __forceinline__ void mma_dot(float (&d)[NR][4], const bf16* __restric
         mma(cur);
     }
     for (; kb < kb1; ++kb) {
-        const uint4 xx = xv ? __ldg(reinterpret_cast<const uint4*>(xr + kb * 32)) : make_uint4(0, 0, 0, 0);
+        uint4 xx[NT];
 #pragma unroll
-        for (int r = 0; r < NR; ++r)
-            kblock(d[r], ld_stream16(wl[r] + kb * 32), ld_stream16(wl[r] + hi_off + kb * 32), xx);
+        for (int t = 0; t < NT; ++t)
+            xx[t] = xv[t] ? __ldg(reinterpret_cast<const uint4*>(xr[t] + kb * 32)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint4 lo = ld_stream16(wl[r] + kb * 32), hi = ld_stream16(wl[r] + hi_off + kb * 32);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) kblock(d[r][t], lo, hi, xx[t]);
+        }
     }
 }
 
 // Warp 0 receives the sum of the S warps' tiles, added in warp order.
 // Returns false in the other warps (which then leave).
-template <int NR>
-__device__ __forceinline__ bool reduce_warps(float (&d)[NR][4], int S) {
-    __shared__ float red[MMA_MAX_WARPS][NR][4][32];
+template <int NR, int NT>
+__device__ __forceinline__ bool reduce_warps(float (&d)[NR][NT][4], int S) {
+    __shared__ float red[MMA_MAX_WARPS][NR * NT][4][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (S == 1) return true;
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) red[warp][r][j][lane] = d[r][j];
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) red[warp][r * NT + t][j][lane] = d[r][t][j];
     __syncthreads();
     if (warp != 0) return false;
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float v = red[0][r][j][lane];
-            for (int w = 1; w < S; ++w) v += red[w][r][j][lane];
-            d[r][j] = v;
-        }
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float v = red[0][r * NT + t][j][lane];
+                for (int w = 1; w < S; ++w) v += red[w][r * NT + t][j][lane];
+                d[r][t][j] = v;
+            }
     return true;
 }
 
@@ -153,9 +176,9 @@ __device__ __forceinline__ void pdl_entry() {
 // STORE / GELU epilogue of gemv_mma_col_k (warp 0): row scale, rotary
 // embedding of the Q and K columns, activation, bf16 store.
 template <int EPI>
-__device__ __forceinline__ void store_rows(const GemvArgs& g, const float (&d)[4], bf16* out, int n0, float rs0,
-                                           float rs1) {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, m0 = 2 * (lane & 3);
+__device__ __forceinline__ void store_rows(const GemvArgs& g, const float (&d)[4], bf16* out, int n0, int mbase,
+                                           float rs0, float rs1) {
+    const int lane = threadIdx.x & 31, gq = lane >> 2, m0 = mbase + 2 * (lane & 3);
     float v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] = d[j] * ((j & 1) ? rs1 : rs0);
@@ -187,7 +210,7 @@ __device__ __forceinline__ void store_rows(const GemvArgs& g, const float (&d)[4
 // Column-parallel: block b = 16 rows of one shard (STORE / GELU, with the
 // optional row scale and rotary embedding) or 16 gate rows + their 16 up
 // rows (SwiGLU).
-template <int EPI>
+template <int EPI, int NT>
 __global__ void __launch_bounds__(MMA_MAX_WARPS * 32) gemv_mma_col_k(GemvArgs g, int S) {
     constexpr int NR = EPI == EPI_SWIGLU ? 2 : 1;
     pdl_entry();
@@ -205,34 +228,42 @@ __global__ void __launch_bounds__(MMA_MAX_WARPS * 32) gemv_mma_col_k(GemvArgs g,
     }
     const bf16* W = (const bf16*)g.W + s * g.w_shard + (long long)n0 * g.K;
     const int nkb = g.K / 32;
-    float d[NR][4];
+    float d[NR][NT][4];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d[r][j] = 0.f;
-    mma_dot<NR>(d, W, W + (long long)g.granule * g.K, g.K, (const bf16*)g.A, g.lda, g.M, warp * nkb / S,
-                (warp + 1) * nkb / S);
-    if (!reduce_warps<NR>(d, S)) return;
-    const int m0 = 2 * c;
-    const float rs0 = g.row_scale && m0 < g.M ? g.row_scale[m0] : 1.f;
-    const float rs1 = g.row_scale && m0 + 1 < g.M ? g.row_scale[m0 + 1] : 1.f;
-    bf16* out = (bf16*)g.out + s * g.out_shard;
-    if constexpr (EPI == EPI_SWIGLU) {
-        const int col0 = (n0 / (2 * g.granule)) * g.granule + n0 % (2 * g.granule) + gq;
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int m = m0 + (j & 1), col = col0 + 8 * (j >> 1);
-            const float rs = (j & 1) ? rs1 : rs0;
-            if (m < g.M) out[(long long)m * g.ldo + col] = __float2bfloat16_rn(silu(d[0][j] * rs) * (d[NR - 1][j] * rs));
+            for (int j = 0; j < 4; ++j) d[r][t][j] = 0.f;
+    mma_dot<NR, NT>(d, W, W + (long long)g.granule * g.K, g.K, (const bf16*)g.A, g.lda, g.M, warp * nkb / S,
+                    (warp + 1) * nkb / S);
+    if (!reduce_warps<NR, NT>(d, S)) return;
+    bf16* out = (bf16*)g.out + s * g.out_shard;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int m0 = 8 * t + 2 * c;
+        const float rs0 = g.row_scale && m0 < g.M ? g.row_scale[m0] : 1.f;
+        const float rs1 = g.row_scale && m0 + 1 < g.M ? g.row_scale[m0 + 1] : 1.f;
+        if constexpr (EPI == EPI_SWIGLU) {
+            const int col0 = (n0 / (2 * g.granule)) * g.granule + n0 % (2 * g.granule) + gq;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int m = m0 + (j & 1), col = col0 + 8 * (j >> 1);
+                const float rs = (j & 1) ? rs1 : rs0;
+                if (m < g.M)
+                    out[(long long)m * g.ldo + col] =
+                        __float2bfloat16_rn(silu(d[0][t][j] * rs) * (d[NR - 1][t][j] * rs));
+            }
+        } else {
+            store_rows<EPI>(g, d[0][t], out, n0, 8 * t, rs0, rs1);
         }
-    } else {
-        store_rows<EPI>(g, d[0], out, n0, rs0, rs1);
     }
 }
 
 // Row-parallel with the fused all-reduce: block b = output features
 // [16b, 16b + 16); warp w takes shard w / Sk and the (w % Sk)-th part of
 // its k range, so the warp-order sum is shard-major.
+template <int NT>
 __global__ void __launch_bounds__(MMA_MAX_WARPS * 32) gemv_mma_row_k(GemvArgs g, int Sk) {
     pdl_entry();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, c = lane & 3;
@@ -240,21 +271,28 @@ __global__ void __launch_bounds__(MMA_MAX_WARPS * 32) gemv_mma_row_k(GemvArgs g,
     const int s = warp / Sk, part = warp % Sk;
     const int n0 = blockIdx.x * 16;
     const int nkb = g.K / 32;
-    float d[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    const bf16* W = (const bf16*)g.W + s * g.w_shard + (long long)n0 * g.K;
-    mma_dot<1>(d, W, W, g.K, (const bf16*)g.A + s * g.a_shard, g.lda, g.M, part * nkb / Sk, (part + 1) * nkb / Sk);
-    if (!reduce_warps<1>(d, S)) return;
+    float d[1][NT][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int n = n0 + gq + 8 * (j >> 1), m = 2 * c + (j & 1);
-        if (m >= g.M) continue;
-        const long long o = (long long)m * g.ldo + n;
-        float v = d[0][j];
-        if (g.residual)
-            v += g.residual_f32 ? ((const float*)g.residual)[o] : __bfloat162float(((const bf16*)g.residual)[o]);
-        ((float*)g.out)[o] = v;
-        if (g.out2) ((bf16*)g.out2)[o] = __float2bfloat16_rn(v);
-    }
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[0][t][j] = 0.f;
+    const bf16* W = (const bf16*)g.W + s * g.w_shard + (long long)n0 * g.K;
+    mma_dot<1, NT>(d, W, W, g.K, (const bf16*)g.A + s * g.a_shard, g.lda, g.M, part * nkb / Sk,
+                   (part + 1) * nkb / Sk);
+    if (!reduce_warps<1, NT>(d, S)) return;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + gq + 8 * (j >> 1), m = 8 * t + 2 * c + (j & 1);
+            if (m >= g.M) continue;
+            const long long o = (long long)m * g.ldo + n;
+            float v = d[0][t][j];
+            if (g.residual)
+                v += g.residual_f32 ? ((const float*)g.residual)[o] : __bfloat162float(((const bf16*)g.residual)[o]);
+            ((float*)g.out)[o] = v;
+            if (g.out2) ((bf16*)g.out2)[o] = __float2bfloat16_rn(v);
+        }
 }
 
 int sm_count_mma() {
@@ -286,30 +324,41 @@ cudaError_t launch(void (*kern)(GemvArgs, int), int blocks, int warps, cudaStrea
 }  // namespace
 
 bool gemv_mma_supported(const GemvArgs& g) {
-    if (g.M < 2 || g.M > 8 || g.K % 32 != 0 || g.lda % 8 != 0 || g.N % 16 != 0 || g.shards < 1) return false;
+    if (g.M < 2 || g.M > GEMV_MMA_MAX_ROWS || g.K % 32 != 0 || g.lda % 8 != 0 || g.N % 16 != 0 || g.shards < 1) return false;
     if (g.reduce) return g.epi == EPI_ROW_REDUCE && g.shards <= MMA_MAX_WARPS;
     if (g.epi == EPI_SWIGLU) return g.granule % 16 == 0 && g.N % (2 * g.granule) == 0;
     return g.epi == EPI_STORE || g.epi == EPI_GELU;
 }
 
-cudaError_t gemv_mma(const GemvArgs& g, cudaStream_t st) {
+namespace {
+
+template <int NT>
+cudaError_t gemv_mma_nt(const GemvArgs& g, cudaStream_t st) {
     const int nkb = g.K / 32;
     const int target_warps = sm_count_mma() * 16;  // enough 16-byte loads in flight to cover HBM latency
     if (g.reduce) {
         int Sk = MMA_MAX_WARPS / g.shards;
         if (Sk < 1) Sk = 1;
         if (Sk > nkb) Sk = nkb;
-        return launch(gemv_mma_row_k, g.N / 16, g.shards * Sk, st, g, Sk);
+        return launch(gemv_mma_row_k<NT>, g.N / 16, g.shards * Sk, st, g, Sk);
     }
     const int blocks = g.shards * (g.epi == EPI_SWIGLU ? g.N / 32 : g.N / 16);
     int S = (target_warps + blocks - 1) / blocks;
     if (S > MMA_MAX_WARPS) S = MMA_MAX_WARPS;
     if (S > nkb) S = nkb;
     if (S < 1) S = 1;
-    void (*kern)(GemvArgs, int) = g.epi == EPI_SWIGLU ? gemv_mma_col_k<EPI_SWIGLU>
-                                  : g.epi == EPI_GELU ? gemv_mma_col_k<EPI_GELU>
-                                                      : gemv_mma_col_k<EPI_STORE>;
+    void (*kern)(GemvArgs, int) = g.epi == EPI_SWIGLU ? gemv_mma_col_k<EPI_SWIGLU, NT>
+                                  : g.epi == EPI_GELU ? gemv_mma_col_k<EPI_GELU, NT>
+                                                      : gemv_mma_col_k<EPI_STORE, NT>;
     return launch(kern, blocks, S, st, g, S);
+}
+
+}  // namespace
+
+cudaError_t gemv_mma(const GemvArgs& g, cudaStream_t st) {
+    if (g.M <= 8) return gemv_mma_nt<1>(g, st);
+    if (g.M <= 16) return gemv_mma_nt<2>(g, st);
+    return gemv_mma_nt<4>(g, st);
 }
 
 }  // namespace tpk

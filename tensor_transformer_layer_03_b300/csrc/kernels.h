@@ -117,16 +117,24 @@ unsigned long long wait_timeout_ns();
 // ---- small-M weight streaming (gemv.cu): same arguments as the GEMM ---------
 typedef TcGemm GemvArgs;
 constexpr int GEMV_MAX_M = 8;
-// Dispatch for 2..8 rows: gemv_mma where it applies; else this CUDA-core
-// loop up to this many rows and the tensor-core GEMM (split-K) above it --
-// at 8 rows the loop is bound by its conversions and FMAs (7B decode step,
-// one B300: 285 us at 8 rows vs 150 us on the tensor-core GEMM).
+// Token rows the tensor-core weight stream (gemv_mma) takes at most; the
+// dispatch prefers it to the tensor-core GEMM over the whole range (7B
+// decode step, tp 2, one B300: 142 vs 175 us at 9 rows, 163 vs 197 at 16,
+// 242 vs 265 at 32 -- the weight bytes are read once either way, and the
+// 128-row GEMM tiles are mostly empty).
+constexpr int GEMV_MMA_MAX_ROWS = 32;
+constexpr int GEMV_MMA_DISPATCH_ROWS = GEMV_MMA_MAX_ROWS;
+// Dispatch for 2..GEMV_MMA_DISPATCH_ROWS rows: gemv_mma where it applies;
+// else this CUDA-core loop up to this many rows and the tensor-core GEMM
+// (split tiles) above it -- at 8 rows the loop is bound by its conversions
+// and FMAs (7B decode step, one B300: 285 us at 8 rows vs 150 us on the
+// tensor-core GEMM).
 constexpr int GEMV_PREFERRED_MAX_M = 4;
 bool gemv_supported(const GemvArgs& g);
 cudaError_t gemv(const GemvArgs& g, int* dev_err, cudaStream_t st);
-// 2..8 rows with the products on the tensor cores (gemv_mma.cu): K a
-// multiple of 32, N a multiple of 16, SwiGLU granule a multiple of 16,
-// row-parallel launches with at most 8 shards.
+// 2..GEMV_MMA_MAX_ROWS rows with the products on the tensor cores
+// (gemv_mma.cu): K a multiple of 32, N a multiple of 16, SwiGLU granule a
+// multiple of 16, row-parallel launches with at most 8 shards.
 bool gemv_mma_supported(const GemvArgs& g);
 cudaError_t gemv_mma(const GemvArgs& g, cudaStream_t st);
 

@@ -218,7 +218,7 @@ static tpk::TcGemm row_gemm(const tp_plan_s* p, int which, const void* in_shards
 static LinearKernel pick_linear(const tp_plan_s* p, const tpk::TcGemm& g) {
     if (p->dtype != TP_BF16) return LK_SIMT;
     const int M = g.M;
-    if (M >= 2 && M <= tpk::GEMV_MAX_M && tpk::gemv_mma_supported(g)) return LK_GEMV_MMA;
+    if (M >= 2 && M <= tpk::GEMV_MMA_DISPATCH_ROWS && tpk::gemv_mma_supported(g)) return LK_GEMV_MMA;
     const bool tc_ok = tpk::tc_gemm_supported(M, g.N, g.K) && (g.epi != tpk::EPI_SWIGLU || g.granule == 32);
     if (tpk::gemv_supported(g) && (M <= tpk::GEMV_PREFERRED_MAX_M || !tc_ok)) return LK_GEMV;
     return tc_ok ? LK_TC : LK_SIMT;

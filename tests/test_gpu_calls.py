@@ -26,6 +26,11 @@ SHAPES = [
     (4096, 32, 11008, 8, 8),
     (512, 8, 1536, 4, 5),
     (256, 4, 1056, 2, 3),    # 16-row gate/up blocks (d_ffn/tp = 528)
+    # 9..32 rows: the weight stream with 2 or 4 groups of 8 token rows
+    (4096, 32, 11008, 2, 16),
+    (1024, 8, 2816, 4, 24),
+    (512, 8, 1536, 2, 32),
+    (256, 4, 1056, 2, 12),
     # one-SM tiles (M <= 128) and the edge of the 256-row SM-pair tiles
     (512, 8, 1536, 2, 128),
     (1024, 8, 2816, 4, 100),

@@ -49,9 +49,10 @@ def _decode_steps(shape, deg, B, P, n, seed):
 
 @pytest.mark.parametrize("B,shape,deg,P,n", [
     (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 6),    # weight-streaming linears (M <= 4)
-    (8, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 90, 3),     # tensor-core linears at 8 rows, split-K
-    (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 5),   # tensor-core linears, split-K
-    (64, I.BlockShape(512, 4, 1536, "swiglu"), 4, 70, 3),     # many sequences, one m-block
+    (8, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 90, 3),     # tensor-core weight stream, 8 rows
+    (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 5),   # tensor-core weight stream, 2 groups of 8 rows
+    (24, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 60, 2),    # tensor-core weight stream, 4 groups (ragged)
+    (64, I.BlockShape(512, 4, 1536, "swiglu"), 4, 70, 3),     # tensor-core GEMM, split tiles of one m-block
 ])
 def test_multistep_decode_growing_cache(tp, B, shape, deg, P, n):
     got, ex, st, k_gpu, k_ref = _decode_steps(shape, deg, B, P, n, seed=11)
@@ -62,8 +63,9 @@ def test_multistep_decode_growing_cache(tp, B, shape, deg, P, n):
 
 
 def test_llama7b_decode_batch16(tp):
-    """The 7B-shaped decode workload with 16 sequences (tensor-core linears
-    at M = 16 with split-K), one step over 1024 cached positions."""
+    """The 7B-shaped decode workload with 16 sequences (the tensor-core
+    weight stream with two groups of 8 token rows), one step over 1024
+    cached positions."""
     shape = I.LLAMA7B
     got, ex, st, _, _ = _decode_steps(shape, 2, 16, 1024, 1, seed=0)
     floor = mean_abs(st, ex)

@@ -81,7 +81,8 @@ def test_llama7b_prefill(tp):
 
 @pytest.mark.parametrize("B,shape,deg,P,n", [
     (4, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 200, 5),    # weight-streaming linears (M <= 4)
-    (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 4),   # tensor-core linears
+    (16, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 130, 4),   # weight stream, 2 groups of 8 rows
+    (40, I.BlockShape(1024, 8, 2816, "swiglu"), 2, 50, 2),    # tensor-core GEMM, split tiles
 ])
 def test_llama_multistep_decode(tp, B, shape, deg, P, n):
     """n single-token steps at positions P..P+n-1 equal one oracle pass of the

@@ -82,7 +82,7 @@ def test_schedule_bounds_and_coverage(tp, shape, degs):
         nscr = plan.linear_scratch_bytes(M)
         s = plan.linear_schedule(row, which, M, nscr, SMS, PAIRS)
         if s.kernel != 0:
-            assert M <= 8 or nscr == 0
+            assert M <= 32 or nscr == 0  # the weight streams take up to 32 rows
             continue
         what = f"d={shape.d_model} tp{deg} M={M} row={row} which={which}"
         ranks = 2 if s.paired else 1
@@ -151,13 +151,18 @@ def test_schedule_query_argument_checks(tp):
 
 
 def test_schedule_few_rows(tp):
-    """Batched decode above 8 rows (7B block, tp 2): a 16-row tile holds 1/8
-    of a full tile's rows, so its partials are 1/8 as large and cutting the
-    48 QKV tiles into parts that fill the SMs pays; at 128 rows (a full
-    tile) the same 48 tiles stay whole."""
+    """Batched decode (7B block, tp 2): up to 32 token rows the linears run
+    the tensor-core weight stream (kernel 1); above, the tensor-core GEMM on
+    128-row tiles.  A 48-row tile holds 3/8 of a full tile's rows, so its
+    partials are 3/8 as large and cutting the 48 QKV tiles into parts that
+    fill the SMs pays; at 128 rows (a full tile) the same 48 tiles stay
+    whole."""
     plan = tp.Plan(4096, 32, 11008, 2)
-    n16 = plan.linear_scratch_bytes(16)
-    s = plan.linear_schedule(0, tp.TP_QKV, 16, n16, SMS, PAIRS)
+    for M in (2, 9, 16, 24, 32):
+        n = plan.linear_scratch_bytes(M)
+        assert {plan.linear_schedule(r, w, M, n, SMS, PAIRS).kernel for r in (0, 1) for w in (0, 1)} == {1}, M
+    n48 = plan.linear_scratch_bytes(48)
+    s = plan.linear_schedule(0, tp.TP_QKV, 48, n48, SMS, PAIRS)
     assert (s.kernel, s.paired, s.tiles) == (0, 0, 48) and s.parts >= 2 and s.items <= SMS
     assert s.whole_tiles == 0 and s.items == 48 * s.parts
     n128 = plan.linear_scratch_bytes(128)
