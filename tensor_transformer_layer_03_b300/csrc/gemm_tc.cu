@@ -126,15 +126,19 @@ struct Params {
     int a_box;
 };
 
+// Layout instantiations of the kernel (SL): 0 plain; 1 sequence-parallel
+// slices of any multiple of 8 rows; 2 slices of a multiple of 128 rows (an
+// A box and an epilogue warp's 32-row block never cross a slice).
+//
 // Element offset of row `row` (column 0) of a row-parallel output / of the
-// residual: plain [M][ldo] (SL false, the kernel instantiation for plain
-// layouts), or slice row / slice_rows at `slice` elements per slice.
-template <bool SL>
+// residual: plain [M][ldo] (SL 0), or slice row / slice_rows at `slice`
+// elements per slice.
+template <int SL>
 __device__ __forceinline__ long long out_row(const Params& p, int row) {
     if (!SL) return (long long)row * p.ldo;
     return (long long)(row / p.slice_rows) * p.out_slice + (long long)(row % p.slice_rows) * p.ldo;
 }
-template <bool SL>
+template <int SL>
 __device__ __forceinline__ long long res_row(const Params& p, int row) {
     if (!SL) return (long long)row * p.ldo;
     return (long long)(row / p.slice_rows) * p.res_slice + (long long)(row % p.slice_rows) * p.ldo;
@@ -144,7 +148,7 @@ __device__ __forceinline__ long long res_row(const Params& p, int row) {
 // row_base a multiple of 32): when no slice boundary can fall inside the
 // block (plain layout, or slices of a multiple of 32 rows) the offsets are
 // the block's first row's plus r * ldo; otherwise each row is mapped.
-template <bool SL>
+template <int SL>
 struct RowMap {
     long long out0, res0;
     int row_base;
@@ -164,11 +168,23 @@ struct RowMap {
 };
 // plain layout: row r of the block is row row_base + r of [M][ldo]
 template <>
-struct RowMap<false> {
+struct RowMap<0> {
     int row_base;
     __device__ __forceinline__ RowMap(const Params&, int rb) : row_base(rb) {}
     __device__ __forceinline__ long long out(const Params& p, int r) const { return (long long)(row_base + r) * p.ldo; }
     __device__ __forceinline__ long long res(const Params& p, int r) const { return (long long)(row_base + r) * p.ldo; }
+};
+// slices of a multiple of 128 rows: the block lies in one slice
+template <>
+struct RowMap<2> {
+    int slice, srow;  // the block's slice and its first row in it
+    __device__ __forceinline__ RowMap(const Params& p, int rb) : slice(rb / p.slice_rows), srow(rb % p.slice_rows) {}
+    __device__ __forceinline__ long long out(const Params& p, int r) const {
+        return (long long)slice * p.out_slice + (long long)(srow + r) * p.ldo;
+    }
+    __device__ __forceinline__ long long res(const Params& p, int r) const {
+        return (long long)slice * p.res_slice + (long long)(srow + r) * p.ldo;
+    }
 };
 
 // Four consecutive finished row-parallel outputs at element offset o of
@@ -329,7 +345,7 @@ __device__ __forceinline__ void col_epilogue(const Params& p, int row, int col, 
 
 // The residual rows [r0, r1) of this warp's 32, columns col0 .. col0+127,
 // pulled into L2 ahead of the epilogue that adds them (one row per lane).
-template <bool SL>
+template <int SL>
 __device__ __forceinline__ void prefetch_residual(const Params& p, int lane, int row_base, int r0, int r1, int col0) {
     if (p.epi != EPI_ROW_REDUCE || p.residual == nullptr || col0 >= p.N) return;
     const int r = r0 + lane, grow = row_base + r;
@@ -410,7 +426,7 @@ __device__ __forceinline__ float4 bf16x4_to_float4(uint2 r) {
 // about a microsecond while the tensor cores stream operands, so the
 // residual of chunk c + 1 is loaded while chunk c is stored (and the rows
 // were pulled into L2 while the MMAs ran).
-template <int RES, bool SL>
+template <int RES, int SL>
 __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, float* stg, int lane, int row_base,
                                              int col0, float* rbuf) {
     constexpr int NC = HALF_N / 32;
@@ -537,7 +553,7 @@ __device__ __noinline__ bool wait_count(const int* cnt, int target, volatile int
 // between parts, `buf` this warp's share of the idle ring: every part's
 // rows and the residual rows are copied into it at once (one memory
 // latency for the whole reduction), then summed from shared memory.
-template <bool SL>
+template <int SL>
 __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, long long pstride, int lane,
                                             int row_base, int r0, int r1, int shard, int col0, float* buf) {
     const int nr = r1 - r0;  // (parts + 1) * nr <= 48 rows of 512 bytes fit FIX_BYTES
@@ -611,7 +627,7 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const float* base, 
 // ... (n of them).  For each, wait (bounded) until all parts of its tile
 // have counted in, reduce this part's rows of the warp's block (those
 // below M) over all parts, and count out.  False when a wait gave up.
-template <class C, bool SL>
+template <class C, int SL>
 __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_units, int kbt, uint32_t rank,
                                           int quarter, int half, int lane, volatile int* abort_flag, float* buf) {
     const int qh = quarter * 2 + half;
@@ -656,9 +672,10 @@ __device__ __noinline__ bool split_fixups(const Params& p, int w0, int n, int n_
 }
 
 // PAIR: 256-row tiles on an SM pair (cta_group::2), else 128-row tiles on
-// one SM.  SL: a sequence-parallel layout (gathered input rows or sliced
-// row-parallel outputs); the plain instantiation has none of its code.
-template <bool PAIR, bool SL>
+// one SM.  SL: the layout (out_row): a sequence-parallel layout (gathered
+// input rows or sliced row-parallel outputs) has its own instantiation, so
+// the plain one carries none of its code.
+template <bool PAIR, int SL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, Params p) {
     using C = GCfg<PAIR>;
@@ -723,6 +740,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tile_coords(p, it.tile, C::GROUP_M, m_blk, shard, n_blk);
                 const int a_row = m_blk * C::TILE_M + (int)rank * A_ROWS;
                 const int w_row = n_blk * BN + (int)rank * C::W_ROWS;
+                // gathered rows in 128-row-aligned slices: one box, its
+                // coordinates fixed for the tile
+                const int a_x = SL == 2 && p.a_box ? a_row % p.slice_rows : a_row;
+                const int a_s = SL == 2 && p.a_box ? a_row / p.slice_rows : 0;
                 for (int kb = it.k0; kb < it.k1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
@@ -735,19 +756,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // both CTAs' copies complete on the issuing CTA's barrier
                         const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
                         if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-                        if (SL && p.a_box)
+                        if (SL == 1 && p.a_box)
                             for (int j = 0; j < A_ROWS; j += p.a_box)  // gathered rows: one box per slice piece
                                 tma_load_3d_pair(sa + j * BK * 2, &tmA, bar0, kk, (a_row + j) % p.slice_rows,
                                                  (a_row + j) / p.slice_rows);
+                        else if (SL == 2 && p.a_box)
+                            tma_load_3d_pair(sa, &tmA, bar0, kk, a_x, a_s);
                         else
                             tma_load_3d_pair(sa, &tmA, bar0, kk, a_row, p.reduce ? s : 0);
                         tma_load_3d_pair(sa + C::A_BYTES, &tmW, bar0, kk, w_row, s);
                     } else {
                         mbar_expect_tx(&full[stage], C::STAGE_BYTES);
-                        if (SL && p.a_box)
+                        if (SL == 1 && p.a_box)
                             for (int j = 0; j < A_ROWS; j += p.a_box)
                                 tma_load_3d(sa + j * BK * 2, &tmA, smem_u32(&full[stage]), kk, (a_row + j) % p.slice_rows,
                                             (a_row + j) / p.slice_rows);
+                        else if (SL == 2 && p.a_box)
+                            tma_load_3d(sa, &tmA, smem_u32(&full[stage]), kk, a_x, a_s);
                         else
                             tma_load_3d(sa, &tmA, smem_u32(&full[stage]), kk, a_row, p.reduce ? s : 0);
                         tma_load_3d(sa + C::A_BYTES, &tmW, smem_u32(&full[stage]), kk, w_row, s);
@@ -1001,7 +1026,7 @@ int pair_slots() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true, false>, &cfg) != cudaSuccess || c <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true, 0>, &cfg) != cudaSuccess || c <= 0) {
             cudaGetLastError();
             c = -1;
         }
@@ -1018,9 +1043,12 @@ cudaError_t set_smem_attr() {
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !done[dev].load()) {
         cudaError_t e =
-            cudaFuncSetAttribute(tc_gemm_kernel<PAIR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<PAIR>::SMEM);
+            cudaFuncSetAttribute(tc_gemm_kernel<PAIR, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<PAIR>::SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tc_gemm_kernel<PAIR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(tc_gemm_kernel<PAIR, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GCfg<PAIR>::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_gemm_kernel<PAIR, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      GCfg<PAIR>::SMEM);
         if (e != cudaSuccess) return e;
         done[dev].store(true);
@@ -1179,8 +1207,9 @@ cudaError_t gemm_launch(const TcGemm& g, int* dev_err, int slots, void* scratch,
     // slices) take their own instantiation, so that the plain one carries
     // neither the per-row slice mapping nor the gathered loads (in the
     // producer's loop they cost the plain 7B prefill linears 5-12 us)
-    if (p.slice_rows > 0) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, true>, tmA, tmW, p);
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, false>, tmA, tmW, p);
+    if (p.slice_rows > 0 && p.slice_rows % A_ROWS == 0) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, 2>, tmA, tmW, p);
+    if (p.slice_rows > 0) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, 1>, tmA, tmW, p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<PAIR, 0>, tmA, tmW, p);
 }
 
 }  // namespace
