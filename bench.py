@@ -427,6 +427,9 @@ def run_sweep(args):
     st = torch.cuda.Stream(device=dev)
     blk, key = None, None
     cpu_done = set()
+    # SM clock and throttle reasons per point (read-only NVML sampling; the
+    # long points run under the power cap, so their clocks matter)
+    clk = ClockSampler(0).start()
     for wl in wls:
         gen = torch.Generator().manual_seed(0)
         pre = wl.name.endswith("_prenorm")
@@ -449,17 +452,21 @@ def run_sweep(args):
         with torch.cuda.stream(st):
             for i in range(3):
                 blk.forward(x, wl.causal, out=y, stream=st)
+            st.synchronize()
+            clk.mark_start()
             for i in range(n):
                 flush.fill_(i & 0xFF)
                 evs[i][0].record(st)
                 blk.forward(x, wl.causal, out=y, stream=st)
                 evs[i][1].record(st)
             st.synchronize()
+            clk.mark_end()
         blk.plan.sync_status(st)
         ms = statistics.median(a.elapsed_time(b) for a, b in evs)
         lin, attn = block_flops(wl)
         tf = (lin + attn) / (ms / 1e3) / 1e12
-        line = {"workload": wl.name, "d_model": wl.shape.d_model, "tp_degree": wl.tp, "batch": wl.batch,
+        line = {"clocks": clk.summary() if clk.nvml else None,
+                "workload": wl.name, "d_model": wl.shape.d_model, "tp_degree": wl.tp, "batch": wl.batch,
                 "seq": wl.seq, "ms_per_block": ms, "tokens_per_s": wl.tokens / (ms / 1e3),
                 "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "steps": n}
         if not args.no_cpu_baseline and not pre and (wl.shape, wl.batch, wl.seq) not in cpu_done:
@@ -511,6 +518,7 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     r = bench_decode(args, dev, batch=1, prenorm=True)
     print(json.dumps({**r, "workload": "llama7b_decode_prenorm_b1"}), flush=True)
+    clk.stop()
     return 0
 
 
@@ -620,8 +628,8 @@ def run_ours(args):
     achieved = stage_flops[dom] / (stage_mean[dom] / 1000.0) / 1e12
     # DRAM traffic (read + write) per launch of each stage's kernel, from one
     # ncu capture of this workload (profiles/tc_gemm_llama7b_prefill.md)
-    traffic = {"column_qkv": 150.04e6, "attention": 50.92e6, "row_o_reduce": 84.70e6,
-               "column_ffn_up_swiglu": 230.69e6, "row_ffn_down_reduce": 266.54e6}
+    traffic = {"column_qkv": 150.30e6, "attention": 50.73e6, "row_o_reduce": 85.17e6,
+               "column_ffn_up_swiglu": 230.71e6, "row_ffn_down_reduce": 267.20e6}
     roofline = {"bound": "tensor", "kernel": stages[dom], "achieved": achieved, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic[stages[dom]],
                 "peak_source": f"{pk['source']} bf16 dense burst (cuBLAS)",
