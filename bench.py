@@ -550,7 +550,7 @@ def run_ours(args):
     u = torch.empty(wl.tp, M, plan.f_l, dtype=torch.bfloat16, device=dev)
     y = torch.empty(M, d, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    # split-tile partials and counters of the linears (zero-filled before first use)
+    # split-tile partials and counters of the linears (contents on entry are ignored)
     gscr = torch.zeros(max(plan.linear_scratch_bytes(M), 16), dtype=torch.uint8, device=dev)
     stages = ["column_qkv", "attention", "row_o_reduce", "column_ffn_up_swiglu", "row_ffn_down_reduce"]
 

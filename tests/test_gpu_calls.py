@@ -77,7 +77,7 @@ def _check(got, ref, dtype, what):
     return assert_close_fp32(got, ref, what)
 
 
-@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "splitk"])
+@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "split"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
 def test_column_qkv(tp, d, H, f, deg, M, dtype, sk):
@@ -98,7 +98,7 @@ def test_column_qkv(tp, d, H, f, deg, M, dtype, sk):
     _check(out, ref, dtype, "QKV")
 
 
-@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "splitk"])
+@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "split"])
 @pytest.mark.parametrize("act", ["swiglu", "gelu"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("d,H,f,deg,M", SHAPES)
@@ -124,7 +124,7 @@ def test_column_ffn_up(tp, d, H, f, deg, M, dtype, act, sk):
     _check(out, ref, dtype, f"FFN-up {act}")
 
 
-@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "splitk"])
+@pytest.mark.parametrize("sk", [False, True], ids=["tiles", "split"])
 @pytest.mark.parametrize("which", ["attn_out", "ffn_down"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("d,H,f,deg,M", SHAPES)

@@ -1,6 +1,6 @@
 """GPU parity of the pre-norm (RMSNorm + RoPE) block against the float64
 oracle's llama_block_forward: prefill on the tensor-core linears (whole
-tiles and split-K), with and without rotation, the 7B shape, multi-step
+and split tiles), with and without rotation, the 7B shape, multi-step
 decode with a growing cache on the weight-streaming and tensor-core linears,
 and a two-layer stack.  Bounds as in test_gpu_block.py: normwise <= 2e-2
 against the exact oracle, mean abs against the oracle's bf16-storage floor
@@ -55,7 +55,7 @@ def _oracles(x, w, H, causal, theta, **kw):
 
 @pytest.mark.parametrize("shape,deg,B,T,theta", [
     (I.BlockShape(512, 8, 1536, "swiglu"), 4, 2, 160, 10000.0),     # whole tiles, ragged tail
-    (I.BlockShape(1024, 8, 2816, "swiglu"), 2, 1, 300, 500000.0),   # split-K linears
+    (I.BlockShape(1024, 8, 2816, "swiglu"), 2, 1, 300, 500000.0),   # split-tile linears
     (I.BlockShape(512, 4, 1536, "swiglu"), 2, 3, 129, 0.0),         # norms only, no rotation
 ])
 def test_llama_prefill(tp, shape, deg, B, T, theta):
