@@ -34,3 +34,22 @@ def test_reference_arm_line():
 
 def test_reference_arm_other_ranks_silent():
     assert _run({"RANK": "1"}) == []
+
+
+def test_clock_sampler_window_and_reasons():
+    """The clocks summary covers only samples inside [mark_start, mark_end]
+    (median SM clock, max clock, union of throttle reasons, sample count),
+    and marks can be set again for the next measured window."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler(0)
+    assert cs.summary()["samples"] == 0
+    cs.samples = [(1.0, 1000, 2032, 500.0, []), (2.0, 1900, 2032, 900.0, ["sw_power_cap"]),
+                  (3.0, 2000, 2032, 950.0, []), (4.0, 2032, 2032, 300.0, ["hw_slowdown"])]
+    cs.t0, cs.t1 = (1.5, None), (3.5, None)
+    s = cs.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 1950.0 and s["sm_max_mhz"] == 2032.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_median"] == 925.0
+    cs.t0, cs.t1 = (3.5, None), (4.5, None)
+    s = cs.summary()
+    assert s["samples"] == 1 and s["reasons"] == ["hw_slowdown"]
