@@ -63,8 +63,9 @@ struct Workspace {
     size_t qkv, attn, hf32, hact, u, scratch, gemm, rs, rope, total;
 };
 
-// Stream-K scratch of the tensor-core GEMMs (bf16 plans, M past the
-// weight-streaming range); 0 when no GEMM of this shape would use it.
+// Split-tile scratch of the tensor-core GEMMs (fp32 partials and their
+// counters; bf16 plans, M past the weight-streaming range); 0 when no GEMM
+// of this shape would use it.
 size_t linear_scratch_bytes(const tp_plan_s* p, long long M) {
     if (p->dtype != TP_BF16 || M <= tpk::GEMV_PREFERRED_MAX_M) return 0;
     return tpk::tc_gemm_scratch_bytes();
