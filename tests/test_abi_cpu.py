@@ -175,6 +175,47 @@ def test_unsupported_head_width(tp):
     assert code == 0
     good = ctypes.c_void_p(0x10000)
     assert tp.tp_attention_heads(h, good, 1, 4, 1, None, None, 0, 0, good, None, 0, None) == 9
+    assert tp.tp_attention_decode_noalloc(h, good, 1, good, good, 8, 3, good, None) == 9
+    tp.tp_plan_destroy(h)
+
+
+def test_noalloc_decode_argument_checks(tp):
+    """The entry point without allocation checks its arguments and the size
+    of its fixed 8 MiB array before anything else: at 32 heads of 128 a
+    batch needs 32 * 64 * 130 * 4 bytes of partials, so 7 rows fit and 8 do
+    not.  A call that passes the checks on a machine without a GPU stops at
+    the device lookup with TP_ERR_CUDA and launches nothing."""
+    code, h = _create(tp, 4096, 32, 11008, 2)
+    assert code == 0
+    P = lambda v: ctypes.c_void_p(v)  # fake device addresses: never dereferenced
+    good, odd = P(0x10000), P(0x10008)
+    N = tp.tp_attention_decode_noalloc
+    assert N(None, good, 1, good, good, 8, 3, good, None) == 1
+    for i in range(4):
+        args = [good, good, good, good]
+        args[i] = None
+        q, k, v, out = args
+        assert N(h, q, 1, k, v, 8, 3, out, None) == 1
+    assert N(h, good, 0, good, good, 8, 3, good, None) == 2     # batch
+    assert N(h, good, 1, good, good, 0, 0, good, None) == 2     # capacity
+    assert N(h, good, 1, good, good, 8, -1, good, None) == 2    # position
+    assert N(h, good, 1, good, good, 8, 8, good, None) == 2     # pos + 1 > cap
+    for i in range(4):
+        args = [good, good, good, good]
+        args[i] = odd
+        q, k, v, out = args
+        assert N(h, q, 1, k, v, 8, 3, out, None) == 7
+    per_row = 32 * 64 * (128 + 2) * 4
+    assert 7 * per_row <= (8 << 20) < 8 * per_row
+    assert N(h, good, 8, good, good, 8, 3, good, None) == 8     # does not fit the array
+    assert N(h, good, 1 << 20, good, good, 8, 3, good, None) == 8
+    try:
+        import torch
+        gpu = torch.cuda.is_available()
+    except Exception:
+        gpu = True
+    if not gpu:
+        assert N(h, good, 7, good, good, 8, 3, good, None) == 10  # fits; no device to look up
     tp.tp_plan_destroy(h)
 
 
