@@ -10,12 +10,13 @@
 // One CTA = one (sequence, head) and two 128-row query tiles that take turns
 // on the tensor core, 320 threads:
 //   warp 0     TMA producer: both Q tiles once, then K_j, V_j (128 keys x
-//              d_head, 128-byte swizzle) into a 3-slot shared-memory ring;
+//              d_head, 128-byte swizzle) into a 5-slot shared-memory ring;
 //   warp 1     TMEM allocator and MMA issuer (one thread):
 //                S_t  = Q_t K_j^T          (M 128, N 128 keys, K = d_head)
 //                O_t += P_t V_j            (M 128, N = d_head, K = 128 keys;
-//                                           V read MN-major straight from the
-//                                           TMA tile, no transpose)
+//                                           P read from TMEM as the A
+//                                           operand, V read MN-major straight
+//                                           from the TMA tile, no transpose)
 //              issued in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
 //              the tensor core works on one tile while the other's softmax
 //              runs;
@@ -23,14 +24,15 @@
 //              query row (its TMEM lane) loads the row of S, applies scale and
 //              mask, updates the running max, rescales its O row in TMEM when
 //              the max grew by more than 2^8 (otherwise the stale max is kept;
-//              the factor cancels in O / l), writes P = 2^(s - m) as bf16 into
-//              a swizzled shared tile (the A operand of the next MMA) and adds
-//              P to its running sum; at the end it normalises O by the sum and
-//              stores the bf16 row.
-// TMEM: S_0 at column 0, S_1 at 128, O_0 at 256, O_1 at 256 + d_head.
-// Every mbarrier wait is bounded (2 s of %globaltimer): on expiry the kernel
-// records a device error, raises a CTA abort flag, drains its MMAs and frees
-// TMEM before returning.
+//              the factor cancels in O / l), writes P = 2^(s - m) as bf16
+//              pairs back over the first 64 columns of its row of S (the A
+//              operand of the next P V) and adds P to its running sum; at the
+//              end it normalises O by the sum and stores the bf16 row.
+// TMEM: S_0 at column 0, S_1 at 128 (P_t over the first 64 columns of S_t),
+// O_0 at 256, O_1 at 256 + d_head.
+// Every mbarrier wait is bounded (tp_set_wait_timeout_ns of %globaltimer, 2 s
+// by default): on expiry the kernel records a device error, raises a CTA
+// abort flag, drains its MMAs and frees TMEM before returning.
 #include <atomic>
 #include <math.h>
 

@@ -11,7 +11,7 @@
 //       -- every shard's partial product is accumulated, in shard order, into
 //       the same TMEM accumulator.
 //
-// Two variants of one persistent kernel (one CTA per SM, 192 threads):
+// Two variants of one persistent kernel (one CTA per SM, 320 threads):
 //  * PAIR (M > 128): clusters of two CTAs on neighbouring SMs compute a
 //    256 x 256 output tile with 2-SM MMAs (tcgen05 .cta_group::2, M = 256):
 //    each CTA stages its own 128 rows of A and 128 of the 256 rows of W, the
@@ -23,9 +23,10 @@
 //   warp 1   TMEM allocator; in the issuing CTA also the MMA thread:
 //            tcgen05.mma kind::f16, K = 16 steps, into one of two 256-column
 //            fp32 TMEM accumulators;
-//   warps 2-5 epilogue: tcgen05.ld of the finished accumulator (each warp its
-//            32-lane quarter), through a per-warp shared staging block so
-//            that global stores are row-contiguous, activation / residual.
+//   warps 2-9 epilogue: tcgen05.ld of the finished accumulator (warp w its
+//            32-lane quarter w % 4 and one 128-column half), through a
+//            per-warp XOR-swizzled shared staging block so that global
+//            stores are row-contiguous, activation / residual.
 // The epilogue of item i overlaps the main loop of item i+1 (two TMEM
 // accumulators = all 512 columns).
 //
