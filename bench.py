@@ -29,6 +29,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s and TFLOP/s (prefill), HBM GB/s (decode) per TP block on 1 B300 vs roofline"
 L2_FLUSH_BYTES = 256 << 20  # > 126 MB L2
+REF_BUDGET_S = 150.0        # reference arm: warm-up + timed oracle calls
+
+
+def workload_config(name, wl, world):
+    """The `config` object of both arms' lines (the same workload, process
+    layout and L2 policy of the timed GPU steps, so the two lines compare)."""
+    s = wl.shape
+    return {"workload": name, "d_model": s.d_model, "n_heads": s.n_heads, "d_ffn": s.d_ffn, "tp_degree": wl.tp,
+            "batch": wl.batch, "seq": wl.seq, "causal": wl.causal, "act": s.act,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": f"GPU steps: L2 flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)"}
 
 
 def block_flops(wl):
@@ -230,30 +241,43 @@ def time_oracle_seq(wl, b):
     return time.perf_counter() - t0
 
 
+def reference_sample(wl, steps, warmup, per_token_s, budget_s=REF_BUDGET_S):
+    """Tokens of sequence 0 that each reference step runs: the whole
+    sequence when warm-up + steps fit the time budget, else the longest
+    causal prefix (a multiple of 64 tokens, at least 64) that does."""
+    fit = int(budget_s / max(1, steps + warmup) / per_token_s)
+    if fit >= wl.seq:
+        return wl.seq
+    return max(64, min(wl.seq, fit // 64 * 64))
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0  # the oracle runs once, on rank 0's host cores
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     from tensor_transformer_layer_03_b300 import inputs as I
     wl = I.WORKLOADS[args.workload]
-    # size each step's sample so that warmup + steps take about 90 s
-    probe = time_oracle(wl, 128, 1)[0]
-    per_token = probe / 128
-    sample = int(90.0 / (args.steps + args.warmup) / per_token) // 64 * 64
-    sample = max(64, min(wl.seq, sample))
+    probe_tokens = min(128, wl.seq)
+    per_token = time_oracle(wl, probe_tokens, 1)[0] / probe_tokens
+    sample = reference_sample(wl, args.steps, args.warmup, per_token)
     times = time_oracle(wl, sample, args.steps, args.warmup)
     total = sum(times)
     value = sample * len(times) / total
     cores = oracle_cores()
-    sample_desc = (f"first {sample} of the {wl.seq} tokens of the same block per step "
-                   f"(causal prefix), float64 numpy oracle")
-    s = wl.shape
+    if sample == wl.seq and wl.batch == 1:
+        sample_desc = f"the whole workload (1 x {wl.seq} tokens) per step, float64 numpy oracle"
+    elif sample == wl.seq:
+        sample_desc = (f"sequence 0 of the {wl.batch} ({wl.seq} tokens) per step, float64 numpy oracle "
+                       "(the sequences are independent)")
+    else:
+        sample_desc = (f"first {sample} of the {wl.seq} tokens of sequence 0 per step (causal prefix), "
+                       "float64 numpy oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "d_model": s.d_model, "n_heads": s.n_heads, "d_ffn": s.d_ffn,
-                   "tp_degree": wl.tp, "batch": wl.batch, "seq": wl.seq, "causal": wl.causal, "act": s.act},
+        "config": workload_config(args.workload, wl, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -705,10 +729,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "d_model": d, "n_heads": s.n_heads, "d_ffn": s.d_ffn,
-                       "tp_degree": wl.tp, "batch": B, "seq": T, "causal": wl.causal, "act": s.act,
-                       "parallelism": f"replicas{world}" if world > 1 else "single",
-                       "l2": "flushed between steps (256 MB write)"},
+            "config": workload_config(args.workload, wl, world),
             "tflops": tflops,
             "tflops_frac_of_peak": tflops / pk["bf16_tflops"],
             "stage_ms": {n: m for n, m in zip(stages, stage_mean)},

@@ -27,6 +27,12 @@ def test_reference_arm_line():
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
     assert d["config"]["workload"] == "tiny_fp32"
+    # the same config object as the GPU arm's line, so the two lines compare
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_transformer_layer_03_b300 import inputs as I
+    assert d["config"] == bench.workload_config("tiny_fp32", I.WORKLOADS["tiny_fp32"], 1)
+    assert d["cpu_baseline"]["sample"].startswith("the whole workload (1 x 64 tokens)")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -53,3 +59,22 @@ def test_clock_sampler_window_and_reasons():
     cs.t0, cs.t1 = (3.5, None), (4.5, None)
     s = cs.summary()
     assert s["samples"] == 1 and s["reasons"] == ["hw_slowdown"]
+
+
+def test_reference_sample_sizing():
+    """The reference arm runs the whole sequence per step when warm-up plus
+    steps fit its time budget, else the longest 64-token-multiple prefix that
+    does (at least 64 tokens)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_transformer_layer_03_b300 import inputs as I
+    wl = I.WORKLOADS["llama7b_prefill"]
+    per_token = 1.0 / 760.0  # the oracle's rate on a 16-core host
+    assert bench.reference_sample(wl, 20, 5, per_token) == wl.seq            # 25 x 2.7 s < 150 s
+    n = bench.reference_sample(wl, 1000, 5, per_token)                        # the default step count
+    assert n == 64
+    n = bench.reference_sample(wl, 80, 5, per_token)                          # 85 x 2.7 s > 150 s
+    assert n % 64 == 0 and 64 <= n < wl.seq and 85 * n * per_token <= bench.REF_BUDGET_S
+    assert 85 * (n + 64) * per_token > bench.REF_BUDGET_S
+    c = bench.workload_config("llama7b_prefill", wl, 4)
+    assert c["parallelism"] == "replicas4" and c["seq"] == 2048 and c["tp_degree"] == 4 and "l2" in c
