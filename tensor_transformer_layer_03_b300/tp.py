@@ -97,8 +97,13 @@ def status_name(code: int) -> str:
 
 
 def _ptr(t):
+    """Device address of a CUDA tensor (None for NULL).  Every buffer
+    argument of the library is device memory, so a host tensor is refused
+    here: a kernel given its address would fault."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -236,7 +241,7 @@ class Plan:
     def stack_forward(self, packed_layers, x, batch, seq, causal, workspace, out_f32, k_caches=None, v_caches=None,
                       cache_cap=0, cache_pos=0, stream=None):
         n = len(packed_layers)
-        arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts]) if ts is not None else None
+        arr = lambda ts: (ctypes.c_void_p * n)(*[_ptr(t).value for t in ts]) if ts is not None else None
         nbytes = workspace.numel() * workspace.element_size()
         check(tp_stack_forward(self.handle, n, arr(packed_layers), _ptr(x), batch, seq, int(causal), arr(k_caches),
                                arr(v_caches), cache_cap, cache_pos, _ptr(workspace), nbytes, _ptr(out_f32),
