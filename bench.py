@@ -177,8 +177,14 @@ def dist_setup(ngpus):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     pg = None
     if world > 1:
+        import datetime
+
         import torch.distributed as dist
-        dist.init_process_group("nccl" if os.environ.get("TP_BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+        backend = "nccl" if os.environ.get("TP_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        # a replica that dies ends the others' next barrier or all-reduce with
+        # an error after this long, instead of leaving them waiting
+        timeout = datetime.timedelta(seconds=float(os.environ.get("TP_BENCH_PG_TIMEOUT_S", "600")))
+        dist.init_process_group(backend, timeout=timeout)
         pg = dist
     return world, rank, local, pg
 
