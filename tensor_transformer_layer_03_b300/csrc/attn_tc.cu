@@ -433,16 +433,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* q = nullptr;
-        cudaDriverEntryPointQueryResult r;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+    static std::atomic<EncodeTiledFn> fn{nullptr};  // racing first calls store the same address
+    EncodeTiledFn f = fn.load();
+    if (!f) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            r == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(q);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<EncodeTiledFn>(p);
+            fn.store(f);
+        }
     }
-    return fn;
+    return f;
 }
 
 // 4-D bf16 tensor [d3][d2][d1][d0] (d0 contiguous), box {64, 128, 1, 1},
