@@ -4,6 +4,7 @@
 // enqueuing anything, then launch the kernels of pack.cu, simt.cu,
 // gemm_tc.cu, attn_tc.cu and decode.cu on the caller's stream.
 #include <atomic>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -107,6 +108,7 @@ tp_status attention_check(const tp_plan_s* p, int batch, int seq_q, const void* 
                           int cache_cap, int cache_pos) {
     if ((k_cache == nullptr) != (v_cache == nullptr)) return TP_ERR_NULL_ARG;
     if (batch <= 0 || seq_q <= 0 || cache_pos < 0) return TP_ERR_INVALID_DIM;
+    if ((long long)batch * seq_q > INT_MAX) return TP_ERR_INVALID_DIM;  // token rows are int in the kernels
     const bool cached = k_cache != nullptr;
     if (!cached && cache_pos != 0) return TP_ERR_INVALID_DIM;
     if (cached && (cache_cap <= 0 || (long long)cache_pos + seq_q > cache_cap)) return TP_ERR_INVALID_DIM;

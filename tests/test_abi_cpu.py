@@ -147,6 +147,9 @@ def test_argument_validation_before_launch(tp):
     assert B(h, good, 1, 4, 1, None, None, 0, 0, good, good, 64, good, None) == 8  # workspace too small
     assert B(h, good, 1, 4, 1, None, None, 0, 0, good, None, 1 << 30, good, None) == 1
     assert B(h, good, 1, 0, 1, None, None, 0, 0, good, good, 1 << 30, good, None) == 2
+    # more than 2^31 - 1 token rows is refused even with a workspace that claims to be large enough
+    assert B(h, good, 1 << 16, 1 << 16, 1, None, None, 0, 0, good, good, (1 << 64) - 1, good, None) == 2
+    assert A(h, good, 1 << 16, 1 << 15, 1, None, None, 0, 0, good, None, 0, None) == 2
     # stack
     S = tp.tp_stack_forward
     arr = (ctypes.c_void_p * 2)(0x10000, 0x20000)
